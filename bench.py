@@ -1,0 +1,454 @@
+"""Benchmark of one paged-decode step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole decode path over one batch of synthetic input
+(for the paged workloads: one pd_decode_attn call, i.e. the unit pass plus the
+merge when the launch splits; for the tiled workload: begin, every step_tile
+call and finalize).  The default workload is the GQA-packed one: 32 sequences
+with lengths uniform in [512, 4096], 16 query heads over 2 KV heads, head dim
+256, block 16, non-split launch through the packed pass.
+
+Metric: KV bytes read per second (live tokens x num_kv_heads x head_dim x 2
+bytes x K and V), whole job; also microseconds per step and the fraction of the
+measured HBM copy peak.  Rank 0 prints one JSON line.
+
+Under torchrun with N > 1 every rank runs an independent replica of the same
+step on its own GPU (the path has no exchange step); the timing is the max
+over ranks and the value is the sum of the ranks' bytes over that time.
+
+`--impl reference` times the FP64 CPU oracle on the same workload on this
+machine's host cores (rank 0 only), each step a bounded sample of sequences.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "paged-decode KV-read GB/s (% of GB300 HBM peak) and us per decode step"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _workload(name):
+    from paged_kv_decode_splitk_gb300 import workloads as W
+    return W.WORKLOADS[name]()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in (self.out or "").splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _traffic_from_profiles(kernel_tag: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    kernel source as it is now (the summary records a hash of the sources)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}__{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_splitk_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    tag = None
+    traffic = None
+    for ln in text.splitlines():
+        if ln.startswith("source_sha256:"):
+            tag = ln.split(":", 1)[1].strip()
+        if ln.startswith("dram_bytes_per_launch:"):
+            traffic = float(ln.split(":", 1)[1].strip())
+    if tag != h.hexdigest()[:16]:
+        return None
+    return traffic
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_decode_splitk_gb300 import api, pd
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = _workload(args.workload)
+    tiled = args.workload == "tiled"
+    kv_bytes = w.kv_bytes
+    stream = torch.cuda.current_stream()
+
+    if not tiled:
+        base = api.PagedInputs(w, dev)
+        n = base.splits()
+        pool_bytes = base.k.numel() * 2 * 2
+        copies = max(2, -(-3 * L2_BYTES // pool_bytes))
+        ks = [base.k] + [base.k.clone() for _ in range(copies - 1)]
+        vs = [base.v] + [base.v.clone() for _ in range(copies - 1)]
+        out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+        wsp = api.workspace(w.num_seqs, w.num_q_heads, w.head_dim, n, dev)
+        launches_per_step = 1 + (1 if n > 1 else 0)
+
+        def step(i):
+            api.decode_attn(base.q, ks[i % copies], vs[i % copies], base.block_table, base.context_lens,
+                            w.inv_sqrt_d, n, w.gqa_pack, out, wsp)
+        l2_note = f"rotating {copies} KV-cache copies ({copies * pool_bytes / 1e6:.0f} MB > 129 MB L2)"
+    else:
+        base = api.TiledInputs(w, dev)
+        n = 1
+        pool_bytes = base.pool.numel() * 2
+        copies = max(2, -(-3 * L2_BYTES // pool_bytes))
+        pools = [base.pool] + [base.pool.clone() for _ in range(copies - 1)]
+        stripe = w.num_kv_heads * w.block_size * w.head_dim
+        t = pd.Tiled(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.tile_capacity)
+        strides = t.scratch_pool_strides()
+        out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+        launches_per_step = 2 + w.num_calls
+
+        def step(i):
+            p = pools[i % copies].view(-1)
+            t.begin(w.num_seqs)
+            for c in range(w.num_calls):
+                t.step(base.q, p, p[stripe:], base.tile_blocks[c], base.tile_counts[c], w.num_seqs,
+                       strides, int(w.last_block_valid_slots[c]))
+            t.finalize(out, w.num_seqs)
+        l2_note = f"rotating {copies} scratch-pool copies ({copies * pool_bytes / 1e6:.0f} MB > 129 MB L2)"
+
+    warmup = max(3, args.warmup)
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if pd.pd_device_status() != 0:
+        raise RuntimeError("device status flags set during warm-up")
+
+    # ---- timed region: K steps back to back, events on the launching stream ----
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        evs[0].record(stream)
+        for i in range(args.steps):
+            step(i)
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if ws > 1:
+        dist.barrier()
+    per_step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    total_ms = evs[0].elapsed_time(evs[-1])
+    t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    total_ms = float(t_max.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * kv_bytes * args.steps / (total_ms / 1e3) / 1e9
+
+    # dominant kernel: the unit pass (the only launch of a packed / non-split step)
+    unit_ms = statistics.median(per_step_ms)
+    peak, peak_kind = _peaks()
+    achieved = kv_bytes / (unit_ms / 1e3) / 1e9
+    kernel_tag = "unit_packed" if w.__dict__.get("gqa_pack") else ("unit_tiled" if tiled else "unit_splitk")
+    traffic = _traffic_from_profiles(kernel_tag, args.workload)
+
+    # ---- end to end: host buffers through the public API ----
+    e2e = None
+    e2e_resident = None
+    if not tiled:
+        def host(t):
+            return t.detach().cpu().pin_memory()
+        hq, hbt, hcl = host(base.q), host(base.block_table), host(base.context_lens)
+        hk, hv = host(base.k), host(base.v)
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dbt, dcl = torch.empty_like(base.q), torch.empty_like(base.block_table), torch.empty_like(base.context_lens)
+        dk, dv = torch.empty_like(base.k), torch.empty_like(base.v)
+
+        def e2e_step(upload_kv):
+            dq.copy_(hq, non_blocking=True)
+            dbt.copy_(hbt, non_blocking=True)
+            dcl.copy_(hcl, non_blocking=True)
+            if upload_kv:
+                dk.copy_(hk, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+            api.decode_attn(dq, dk if upload_kv else ks[0], dv if upload_kv else vs[0], dbt, dcl,
+                            w.inv_sqrt_d, n, w.gqa_pack, out, wsp)
+            hout.copy_(out, non_blocking=True)
+
+        def timed(upload_kv, k):
+            for _ in range(3):
+                e2e_step(upload_kv)
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(k):
+                e2e_step(upload_kv)
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / k
+
+        small_in = hq.numel() * 2 + hbt.numel() * 4 + hcl.numel() * 4
+        out_b = hout.numel() * 2
+        ms_kv = timed(True, max(3, min(args.steps, 20)))
+        ms_res = timed(False, args.steps)
+        e2e = {"value": round(ws * kv_bytes / (ms_kv / 1e3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(ms_kv, 5),
+               "h2d_bytes_per_step": int(small_in + hk.numel() * 2 + hv.numel() * 2),
+               "d2h_bytes_per_step": int(out_b),
+               "note": "host buffers: q, block table, context lengths and the whole K/V pool copied "
+                       "from pinned host memory every step, output read back"}
+        e2e_resident = {"value": round(ws * kv_bytes / (ms_res / 1e3) / 1e9, 2), "unit": "GB/s",
+                        "ms_per_step": round(ms_res, 5), "h2d_bytes_per_step": int(small_in),
+                        "d2h_bytes_per_step": int(out_b),
+                        "note": "KV cache resident in HBM (decode-serving form): only q, tables and "
+                                "the output cross the host link"}
+    if pd.pd_device_status() != 0:
+        raise RuntimeError("device status flags set during the timed region")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.workload, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": warmup,
+            "ms_per_step": round(ms_per_step, 6),
+            "us_per_step": round(ms_per_step * 1e3, 3),
+            "hbm_frac": round(value / ws / peak, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) BF16 q/K/V, seeded lengths and block tables)",
+            "config": {
+                "workload": w.name,
+                "num_seqs": w.num_seqs,
+                "num_q_heads": w.num_q_heads,
+                "num_kv_heads": w.num_kv_heads,
+                "head_dim": w.head_dim,
+                "block_size": w.block_size,
+                "num_splits": n,
+                "gqa_pack": bool(w.__dict__.get("gqa_pack", False)),
+                "kv_bytes_per_step": kv_bytes,
+                "tokens": int(w.context_lens.sum()) if not tiled else w.kv_tokens,
+                "l2": l2_note,
+                "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            },
+            "roofline": {
+                "bound": "hbm",
+                "kernel": kernel_tag,
+                "achieved": round(achieved, 2),
+                "peak": peak,
+                "peak_kind": peak_kind,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "per_launch_us": round(unit_ms * 1e3, 3),
+            },
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "e2e": e2e,
+            "e2e_resident_kv": e2e_resident,
+            "cpu_baseline": cpu,
+            "wall_s_timed": round(wall, 4),
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def _oracle_step(w, seqs):
+    import oracle
+    if hasattr(w, "context_lens"):
+        return oracle.decode_attn(w.q[seqs], w.k_cache, w.v_cache, w.block_table[seqs],
+                                  w.context_lens[seqs], w.inv_sqrt_d)
+    from paged_kv_decode_splitk_gb300 import workloads as W
+    kf, vf = W.scratch_pool_views(w.pool)
+    return oracle.tiled_attn(w.q[seqs], kf, vf, w.tile_blocks[:, seqs], w.tile_block_counts[:, seqs],
+                             w.last_block_valid_slots, w.num_kv_heads, w.block_size,
+                             oracle.scratch_pool_strides(w.num_kv_heads, w.head_dim, w.block_size))
+
+
+def _seq_bytes(w, seqs):
+    if hasattr(w, "context_lens"):
+        return int(w.context_lens[seqs].astype("int64").sum()) * w.num_kv_heads * w.head_dim * 4
+    bs = w.block_size
+    tok = 0
+    for c in range(w.num_calls):
+        lb = int(w.last_block_valid_slots[c])
+        for s in seqs:
+            cnt = int(w.tile_block_counts[c, s])
+            if cnt:
+                tok += (cnt - 1) * bs + (lb if 1 <= lb < bs else bs)
+    return tok * w.num_kv_heads * w.head_dim * 4
+
+
+def _sample_seqs(w, budget_s):
+    """Sequences (in a fixed seeded order) whose oracle time fits the budget, estimated
+    from a first timed sequence."""
+    import numpy as np
+    order = np.random.default_rng(123).permutation(w.num_seqs)
+    t0 = time.perf_counter()
+    _oracle_step(w, order[:1])
+    dt = max(time.perf_counter() - t0, 1e-4)
+    rate = _seq_bytes(w, order[:1]) / dt
+    target = rate * budget_s
+    acc, chosen = 0, []
+    for s in order:
+        b = _seq_bytes(w, [s])
+        if chosen and acc + b > target:
+            break
+        chosen.append(int(s))
+        acc += b
+    return sorted(chosen)
+
+
+def cpu_baseline(w, workload, budget_s=10.0):
+    seqs = _sample_seqs(w, budget_s)
+    t0 = time.perf_counter()
+    _oracle_step(w, seqs)
+    dt = time.perf_counter() - t0
+    b = _seq_bytes(w, seqs)
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(seqs)} of {w.num_seqs} sequences of {workload} ({b / 1e6:.1f} MB of K/V), "
+                      f"FP64 C oracle, single thread, {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    w = _workload(args.workload)
+    budget = min(args.cpu_seconds, 150.0 / max(1, args.steps + max(3, args.warmup)))
+    seqs = _sample_seqs(w, budget)
+    b = _seq_bytes(w, seqs)
+    for _ in range(max(3, args.warmup)):
+        _oracle_step(w, seqs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(w, seqs)
+    dt = time.perf_counter() - t0
+    value = b * args.steps / dt / 1e9
+    ms = dt / args.steps * 1e3
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) BF16 q/K/V, seeded lengths and block tables)",
+        "config": {"workload": w.name, "sample_seqs": len(seqs), "kv_bytes_per_step": b},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{len(seqs)} of {w.num_seqs} sequences per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_packed",
+                    choices=["tiny", "gqa_packed", "long_context", "large_batch", "tiled"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,734 @@
+// pd_api.cu -- the C ABI of libpd (declared in include/pd.h): argument
+// validation, the split-K launch-geometry policy, TMA tensor-map encoding,
+// kernel dispatch and the tiled state.  Host code; the kernels live in
+// pd_unit_d*.cu and pd_small.cu.
+#include <cudaTypedefs.h>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cctype>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pd.h"
+#include "pd_internal.h"
+
+namespace {
+
+// ---- errors -------------------------------------------------------------------
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok() {
+    g_err[0] = '\0';
+    return PD_OK;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(PD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---- text -----------------------------------------------------------------------
+std::string trim_lower(const char *text) {
+    std::string s = text ? text : "";
+    size_t a = 0, b = s.size();
+    while (a < b && std::isspace(static_cast<unsigned char>(s[a]))) ++a;
+    while (b > a && std::isspace(static_cast<unsigned char>(s[b - 1]))) --b;
+    std::string out = s.substr(a, b - a);
+    for (char &c : out) c = static_cast<char>(std::tolower(static_cast<unsigned char>(c)));
+    return out;
+}
+
+bool is_off_word(const std::string &w) { return w == "0" || w == "off" || w == "false" || w == "no"; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- device status word ------------------------------------------------------------
+__device__ unsigned int g_status;
+
+std::mutex g_status_mu;
+unsigned int *g_status_ptr[64] = {nullptr};
+
+unsigned int *status_ptr(int *err) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = cuda_fail(e == cudaSuccess ? cudaErrorInvalidDevice : e, "cudaGetDevice");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status);
+        if (e != cudaSuccess) {
+            *err = cuda_fail(e, "cudaGetSymbolAddress(status)");
+            return nullptr;
+        }
+        g_status_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    *err = PD_OK;
+    return g_status_ptr[dev];
+}
+
+// ---- TMA tensor maps -------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else if (g_encode_err == cudaSuccess)
+            g_encode_err = cudaErrorSymbolNotFound;
+    });
+    return g_encode;
+}
+
+// A 4-D view of one K (or V) pool: dim 0 the head_dim columns, then the token
+// and KV-head axes in increasing stride order, then the block axis.  Box: 64
+// columns x 16 tokens x 1 head x 1 block, 128-byte swizzle; out-of-range
+// coordinates read zeros.  *tok_dim receives the dimension holding tokens.
+int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim, int block_size,
+                  int num_kv_heads, long long num_blocks, long long blk_stride, long long tok_stride,
+                  long long kvh_stride) {
+    auto enc = encoder();
+    if (!enc) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled entry point");
+    const bool tok_first = tok_stride <= kvh_stride;
+    cuuint64_t dims[4];
+    cuuint64_t strides[3];
+    cuuint32_t box[4];
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    dims[0] = static_cast<cuuint64_t>(head_dim);
+    box[0] = pd::kBoxCols;
+    if (tok_first) {
+        dims[1] = block_size;
+        strides[0] = static_cast<cuuint64_t>(tok_stride) * 2;
+        box[1] = pd::kTileTokens;
+        dims[2] = num_kv_heads;
+        strides[1] = static_cast<cuuint64_t>(kvh_stride) * 2;
+        box[2] = 1;
+    } else {
+        dims[1] = num_kv_heads;
+        strides[0] = static_cast<cuuint64_t>(kvh_stride) * 2;
+        box[1] = 1;
+        dims[2] = block_size;
+        strides[1] = static_cast<cuuint64_t>(tok_stride) * 2;
+        box[2] = pd::kTileTokens;
+    }
+    dims[3] = static_cast<cuuint64_t>(num_blocks);
+    strides[2] = static_cast<cuuint64_t>(blk_stride) * 2;
+    box[3] = 1;
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PD_ERR_INVALID,
+                    "cuTensorMapEncodeTiled rejected the K/V view (error %d): base %p, strides "
+                    "(blk %lld, tok %lld, kvh %lld) elements",
+                    static_cast<int>(r), base, blk_stride, tok_stride, kvh_stride);
+    *tok_dim = tok_first ? 1 : 2;
+    return PD_OK;
+}
+
+// ---- launch choices ----------------------------------------------------------------
+// Stages per warp of the unit pipeline: about 64 KB of K/V in flight per CTA
+// so that two or three CTAs share an SM.
+int g_debug_stages = 0;
+int g_debug_cluster = 0;
+
+int default_stages(int dpad) {
+    if (g_debug_stages > 0) return g_debug_stages;
+    switch (dpad) {
+        case 64: return 6;
+        case 128: return 3;
+        default: return 1;
+    }
+}
+
+// CTAs per packed unit: the packed pass has only num_kv_heads * num_seqs
+// units, so each is spread over a cluster that merges through distributed
+// shared memory.  A build constant (it fixes the summation order).
+constexpr int kPackCluster = 4;
+
+int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
+
+template <int MODE>
+cudaError_t dispatch_unit(int dpad, int gn, bool packed, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const pd::UnitParams &p, int grid_x, int smem, cudaStream_t st) {
+    if (packed) return pd::launch_unit<256, 1, pd::kModePaged, true>(tk, tv, p, grid_x, smem, st);
+    if (dpad == 64)
+        return gn == 1 ? pd::launch_unit<64, 1, MODE, false>(tk, tv, p, grid_x, smem, st)
+                       : pd::launch_unit<64, 2, MODE, false>(tk, tv, p, grid_x, smem, st);
+    if (dpad == 128)
+        return gn == 1 ? pd::launch_unit<128, 1, MODE, false>(tk, tv, p, grid_x, smem, st)
+                       : pd::launch_unit<128, 2, MODE, false>(tk, tv, p, grid_x, smem, st);
+    return gn == 1 ? pd::launch_unit<256, 1, MODE, false>(tk, tv, p, grid_x, smem, st)
+                   : pd::launch_unit<256, 2, MODE, false>(tk, tv, p, grid_x, smem, st);
+}
+
+int check_shape(int num_q_heads, int num_kv_heads, int head_dim, int block_size) {
+    if (num_kv_heads <= 0 || num_q_heads <= 0)
+        return fail(PD_ERR_INVALID, "num_q_heads (%d) and num_kv_heads (%d) must be positive",
+                    num_q_heads, num_kv_heads);
+    if (num_q_heads % num_kv_heads != 0)
+        return fail(PD_ERR_INVALID, "num_kv_heads (%d) must divide num_q_heads (%d)", num_kv_heads,
+                    num_q_heads);
+    if (head_dim > PD_MAX_HEAD_DIM)
+        return fail(PD_ERR_INVALID, "head_dim %d exceeds PD_MAX_HEAD_DIM=%d", head_dim, PD_MAX_HEAD_DIM);
+    if (head_dim < 8 || head_dim % 8 != 0)
+        return fail(PD_ERR_UNSUPPORTED, "head_dim %d: this build needs a positive multiple of 8",
+                    head_dim);
+    if (block_size < 16 || block_size > 256 || block_size % 16 != 0)
+        return fail(PD_ERR_UNSUPPORTED,
+                    "block_size %d: this build needs a multiple of 16 in [16, 256]", block_size);
+    return PD_OK;
+}
+
+}  // namespace
+
+struct pd_tiled {
+    pd_tiled_dims dims;
+    float *m;
+    float *l;
+    float *o;
+    int device;
+};
+
+namespace {
+std::atomic<int> g_fail_allocs{0};
+}
+
+extern "C" {
+
+const char *pd_last_error(void) { return g_err; }
+
+int pd_build_info(int *max_splits, int *pack_width, int *pack_head_dim, int *min_kv_per_split) {
+    if (max_splits) *max_splits = PD_MAX_DECODE_SPLITS;
+    if (pack_width) *pack_width = pd::kernel_pack_width();
+    if (pack_head_dim) *pack_head_dim = pd::kernel_pack_head_dim();
+    if (min_kv_per_split) *min_kv_per_split = PD_MIN_KV_PER_SPLIT;
+    return ok();
+}
+
+// ---- policy -------------------------------------------------------------------------
+
+int pd_parse_policy(const char *text, int *policy, int *pin) {
+    if (!text || !policy || !pin) return fail(PD_ERR_INVALID, "pd_parse_policy: null argument");
+    const std::string w = trim_lower(text);
+    if (w == "legacy") {
+        *policy = PD_POLICY_LEGACY;
+        *pin = 0;
+        return ok();
+    }
+    if (w == "auto") {
+        *policy = PD_POLICY_AUTO;
+        *pin = 0;
+        return ok();
+    }
+    if (is_off_word(w)) {
+        *policy = PD_POLICY_PINNED;
+        *pin = 1;
+        return ok();
+    }
+    if (!w.empty() && w.find_first_not_of("0123456789") == std::string::npos) {
+        // A decimal count, clamped to 1..MAX (saturating: long strings are large counts).
+        long long v = 0;
+        for (char c : w) {
+            v = v * 10 + (c - '0');
+            if (v > PD_MAX_DECODE_SPLITS) {
+                v = PD_MAX_DECODE_SPLITS;
+                break;
+            }
+        }
+        *policy = PD_POLICY_PINNED;
+        *pin = static_cast<int>(v < 1 ? 1 : v);
+        return ok();
+    }
+    return fail(PD_ERR_INVALID, "not a split-K policy: '%s'", text);
+}
+
+int pd_parse_gqa_pack(const char *text, int *enabled) {
+    if (!text || !enabled) return fail(PD_ERR_INVALID, "pd_parse_gqa_pack: null argument");
+    const std::string w = trim_lower(text);
+    if (w == "1" || w == "on" || w == "true" || w == "yes") {
+        *enabled = 1;
+        return ok();
+    }
+    if (is_off_word(w)) {
+        *enabled = 0;
+        return ok();
+    }
+    return fail(PD_ERR_INVALID, "not a GQA-pack switch: '%s'", text);
+}
+
+int pd_resolve_policy(const char *declared, const char *override_text, int *policy, int *pin) {
+    if (!policy || !pin) return fail(PD_ERR_INVALID, "pd_resolve_policy: null argument");
+    int pol = 0, pn = 0;
+    if (override_text && pd_parse_policy(override_text, &pol, &pn) == PD_OK) {
+        *policy = pol;
+        *pin = pn;
+        return ok();
+    }
+    if (declared && pd_parse_policy(declared, &pol, &pn) == PD_OK) {
+        *policy = pol;
+        *pin = pn;
+        return ok();
+    }
+    *policy = PD_POLICY_LEGACY;
+    *pin = 0;
+    return ok();
+}
+
+int pd_policy_from_env(const char *declared, int *policy, int *pin) {
+    return pd_resolve_policy(declared, std::getenv("PD_ATTN_DECODE_SPLITK"), policy, pin);
+}
+
+int pd_gqa_pack_enabled(void) {
+    static std::once_flag once;
+    static int enabled = 0;  // declared state: off
+    std::call_once(once, [] {
+        const char *v = std::getenv("PD_ATTN_DECODE_GQA_PACK");
+        int e = 0;
+        if (v && pd_parse_gqa_pack(v, &e) == PD_OK) enabled = e;
+    });
+    return enabled;
+}
+
+int pd_split_ref_seqs(int num_seqs, int max_decode_seqs) {
+    return num_seqs > max_decode_seqs ? num_seqs : max_decode_seqs;
+}
+
+int pd_legacy_splits(int sm_count, int num_q_heads, int ref_seqs) {
+    if (sm_count <= 0 || num_q_heads <= 0 || ref_seqs <= 0)
+        return fail(PD_ERR_INVALID, "legacy_splits: sm_count %d, num_q_heads %d, ref_seqs %d",
+                    sm_count, num_q_heads, ref_seqs);
+    const long long ctas = static_cast<long long>(num_q_heads) * ref_seqs;
+    ok();
+    return ctas >= sm_count ? 1 : static_cast<int>(sm_count / ctas);
+}
+
+int pd_auto_splits(int sm_count, int num_q_heads) {
+    if (sm_count <= 0 || num_q_heads <= 0)
+        return fail(PD_ERR_INVALID, "auto_splits: sm_count %d, num_q_heads %d", sm_count, num_q_heads);
+    const long long want =
+        (static_cast<long long>(PD_SPLITK_TARGET_WAVES) * sm_count + num_q_heads - 1) / num_q_heads;
+    ok();
+    return static_cast<int>(want < 1 ? 1 : (want > PD_MAX_DECODE_SPLITS ? PD_MAX_DECODE_SPLITS : want));
+}
+
+int pd_num_splits(int policy, int pin, int sm_count, int num_q_heads, int num_seqs,
+                  int max_decode_seqs) {
+    switch (policy) {
+        case PD_POLICY_LEGACY:
+            if (num_seqs < 0 || max_decode_seqs < 0)
+                return fail(PD_ERR_INVALID, "num_splits: negative batch");
+            return pd_legacy_splits(sm_count, num_q_heads, pd_split_ref_seqs(num_seqs, max_decode_seqs));
+        case PD_POLICY_AUTO:
+            return pd_auto_splits(sm_count, num_q_heads);
+        case PD_POLICY_PINNED:
+            ok();
+            return pin < 1 ? 1 : (pin > PD_MAX_DECODE_SPLITS ? PD_MAX_DECODE_SPLITS : pin);
+        default:
+            return fail(PD_ERR_INVALID, "unknown split-K policy %d", policy);
+    }
+}
+
+size_t pd_workspace_bytes(int rows, int num_q_heads, int head_dim, int num_splits) {
+    if (rows <= 0 || num_q_heads <= 0 || head_dim <= 0 || num_splits <= 0) return 0;
+    return static_cast<size_t>(rows) * num_q_heads * num_splits * (head_dim + 2) * sizeof(float);
+}
+
+int pd_gqa_pack_shape_ok(int num_q_heads, int num_kv_heads, int head_dim) {
+    return num_kv_heads > 0 && num_q_heads == num_kv_heads * PD_GQA_PACK_WIDTH &&
+           head_dim == PD_GQA_PACK_HEAD_DIM;
+}
+
+int pd_gqa_pack_ctas(int num_kv_heads, int num_seqs) { return num_kv_heads * num_seqs; }
+
+int pd_split_chunk_tokens(int context_len, int num_splits, int block_size) {
+    if (context_len < 0 || num_splits <= 0 || block_size <= 0)
+        return fail(PD_ERR_INVALID, "split_chunk_tokens: context_len %d, num_splits %d, block_size %d",
+                    context_len, num_splits, block_size);
+    ok();
+    return pd::split_chunk_tokens(context_len, num_splits, block_size, PD_MIN_KV_PER_SPLIT);
+}
+
+// ---- paged decode ----------------------------------------------------------------------
+
+int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_table, int max_blocks_per_seq,
+                   const int32_t *context_lens, void *out, int num_seqs, int num_q_heads,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   float inv_sqrt_d, int num_splits, void *workspace, size_t workspace_bytes,
+                   int gqa_pack, void *stream) {
+    if (gqa_pack != 0 && gqa_pack != 1) return fail(PD_ERR_INVALID, "gqa_pack must be 0 or 1");
+    if (gqa_pack) {
+        if (num_splits != 1)
+            return fail(PD_NOT_APPLICABLE, "GQA-packed pass serves non-split launches only (num_splits=%d)",
+                        num_splits);
+        if (!pd_gqa_pack_shape_ok(num_q_heads, num_kv_heads, head_dim))
+            return fail(PD_NOT_APPLICABLE,
+                        "GQA-packed pass needs num_q_heads == %d*num_kv_heads and head_dim == %d "
+                        "(got %d, %d, %d)",
+                        PD_GQA_PACK_WIDTH, PD_GQA_PACK_HEAD_DIM, num_q_heads, num_kv_heads, head_dim);
+    }
+    int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size);
+    if (rc != PD_OK) return rc;
+    if (num_seqs < 0) return fail(PD_ERR_INVALID, "num_seqs %d < 0", num_seqs);
+    if (num_splits < 1 || num_splits > 4096)
+        return fail(PD_ERR_INVALID, "num_splits %d outside 1..4096", num_splits);
+    if (!std::isfinite(inv_sqrt_d)) return fail(PD_ERR_INVALID, "inv_sqrt_d is not finite");
+    if (num_seqs == 0) return ok();
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out)
+        return fail(PD_ERR_INVALID, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return fail(PD_ERR_INVALID, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if (max_blocks_per_seq <= 0 || num_blocks <= 0)
+        return fail(PD_ERR_INVALID, "max_blocks_per_seq (%d) and num_blocks (%d) must be positive",
+                    max_blocks_per_seq, num_blocks);
+    if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffLL)
+        return fail(PD_ERR_INVALID, "max_blocks_per_seq * block_size overflows int32");
+    if (num_splits > 1) {
+        const size_t need = pd_workspace_bytes(num_seqs, num_q_heads, head_dim, num_splits);
+        if (!workspace || workspace_bytes < need)
+            return fail(PD_ERR_WORKSPACE, "split-K workspace of %zu bytes needed, %zu given%s", need,
+                        workspace ? workspace_bytes : static_cast<size_t>(0), workspace ? "" : " (null)");
+        if (!aligned16(workspace)) return fail(PD_ERR_INVALID, "workspace must be 16-byte aligned");
+    }
+
+    const int G = num_q_heads / num_kv_heads;
+    const bool packed = gqa_pack == 1;
+    const int dpad = packed ? PD_GQA_PACK_HEAD_DIM : dpad_for(head_dim);
+    const int gn = packed ? 1 : (G <= 8 ? 1 : 2);
+    const int rows = 8 * gn;
+    const int qtiles = (G + rows - 1) / rows;
+    int cluster = packed ? kPackCluster : 1;
+    if (g_debug_cluster > 0) cluster = g_debug_cluster;
+    const int stages = default_stages(dpad);
+    const long long grid = static_cast<long long>(num_seqs) * num_kv_heads * qtiles * num_splits * cluster;
+    if (grid > 0x7fffffffLL) return fail(PD_ERR_INVALID, "launch too large (%lld CTAs)", grid);
+
+    int err = PD_OK;
+    unsigned int *status = status_ptr(&err);
+    if (!status) return err;
+
+    CUtensorMap tk, tv;
+    int tok_dim = 1;
+    const long long kvh_s = head_dim, tok_s = static_cast<long long>(num_kv_heads) * head_dim;
+    const long long blk_s = tok_s * block_size;
+    rc = encode_kv_map(&tk, &tok_dim, k_cache, head_dim, block_size, num_kv_heads, num_blocks, blk_s,
+                       tok_s, kvh_s);
+    if (rc != PD_OK) return rc;
+    rc = encode_kv_map(&tv, &tok_dim, v_cache, head_dim, block_size, num_kv_heads, num_blocks, blk_s,
+                       tok_s, kvh_s);
+    if (rc != PD_OK) return rc;
+
+    pd::UnitParams p = {};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.context_lens = context_lens;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.num_splits = num_splits;
+    p.min_kv_per_split = PD_MIN_KV_PER_SPLIT;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    float *ws = static_cast<float *>(workspace);
+    p.ws_o = num_splits > 1 ? ws : nullptr;
+    p.ws_ml = num_splits > 1 ? ws + static_cast<size_t>(num_seqs) * num_q_heads * num_splits * head_dim
+                             : nullptr;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = G;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.qtiles = qtiles;
+    p.cluster = cluster;
+    p.stages = stages;
+    p.tok_dim = tok_dim;
+    p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
+    p.status = status;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int smem = pd::unit_smem_bytes(dpad, rows, stages);
+    cudaError_t e = dispatch_unit<pd::kModePaged>(dpad, gn, packed, tk, tv, p, static_cast<int>(grid),
+                                                  smem, st);
+    if (e != cudaSuccess) return cuda_fail(e, "unit kernel launch");
+    if (num_splits > 1) {
+        pd::MergeParams mp = {};
+        mp.context_lens = context_lens;
+        mp.ws_o = p.ws_o;
+        mp.ws_ml = p.ws_ml;
+        mp.out = p.out;
+        mp.num_seqs = num_seqs;
+        mp.num_q_heads = num_q_heads;
+        mp.head_dim = head_dim;
+        mp.num_splits = num_splits;
+        mp.block_size = block_size;
+        mp.min_kv_per_split = PD_MIN_KV_PER_SPLIT;
+        mp.max_tokens = max_blocks_per_seq * block_size;
+        e = pd::launch_merge(mp, st, true);
+        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    }
+    return ok();
+}
+
+// ---- tiled ----------------------------------------------------------------------------------
+
+int pd_tiled_validate(const pd_tiled_dims *d) {
+    if (!d) return fail(PD_ERR_INVALID, "null dims");
+    if (d->max_seqs < 0 || d->tile_capacity < 0)
+        return fail(PD_ERR_INVALID, "max_seqs (%d) and tile_capacity (%d) must be >= 0", d->max_seqs,
+                    d->tile_capacity);
+    int rc = check_shape(d->num_q_heads, d->num_kv_heads, d->head_dim, d->block_size);
+    if (rc != PD_OK) return rc;
+    return ok();
+}
+
+int pd_tiled_state_bytes(const pd_tiled_dims *d, size_t *m_bytes, size_t *l_bytes, size_t *o_bytes,
+                         size_t *output_bytes) {
+    if (!d || d->max_seqs < 0 || d->num_q_heads < 0 || d->head_dim < 0)
+        return fail(PD_ERR_INVALID, "bad dims");
+    const size_t nq = static_cast<size_t>(d->max_seqs) * d->num_q_heads;
+    if (m_bytes) *m_bytes = nq * 4;
+    if (l_bytes) *l_bytes = nq * 4;
+    if (o_bytes) *o_bytes = nq * d->head_dim * 4;
+    if (output_bytes) *output_bytes = nq * d->head_dim * 2;
+    return ok();
+}
+
+int pd_tiled_create(const pd_tiled_dims *dims, pd_tiled **out) {
+    if (!out) return fail(PD_ERR_INVALID, "null out");
+    *out = nullptr;
+    int rc = pd_tiled_validate(dims);
+    if (rc != PD_OK) return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    size_t mb = 0, lb = 0, ob = 0;
+    pd_tiled_state_bytes(dims, &mb, &lb, &ob, nullptr);
+    pd_tiled *t = new pd_tiled();
+    t->dims = *dims;
+    t->device = dev;
+    float **bufs[3] = {&t->m, &t->l, &t->o};
+    size_t sizes[3] = {mb, lb, ob};
+    for (int i = 0; i < 3; ++i) {
+        void *p = nullptr;
+        int inject = g_fail_allocs.load();
+        while (inject > 0 && !g_fail_allocs.compare_exchange_weak(inject, inject - 1)) {
+        }
+        if (inject > 0) {
+            e = cudaErrorMemoryAllocation;
+        } else {
+            e = cudaMalloc(&p, sizes[i] > 0 ? sizes[i] : 16);
+        }
+        if (e != cudaSuccess) {
+            cudaFree(t->m);
+            cudaFree(t->l);
+            cudaFree(t->o);
+            delete t;
+            return fail(PD_ERR_ALLOC, "tiled state allocation of %zu bytes failed: %s", sizes[i],
+                        cudaGetErrorString(e));
+        }
+        *bufs[i] = static_cast<float *>(p);
+    }
+    *out = t;
+    return ok();
+}
+
+void pd_tiled_destroy(pd_tiled *t) {
+    if (!t) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(t->device);
+    cudaDeviceSynchronize();
+    cudaFree(t->m);
+    cudaFree(t->l);
+    cudaFree(t->o);
+    cudaSetDevice(cur);
+    delete t;
+}
+
+int pd_tiled_get_dims(const pd_tiled *t, pd_tiled_dims *dims) {
+    if (!t || !dims) return fail(PD_ERR_INVALID, "null argument");
+    *dims = t->dims;
+    return ok();
+}
+
+int pd_tiled_state(const pd_tiled *t, void **m, void **l, void **o) {
+    if (!t) return fail(PD_ERR_INVALID, "null handle");
+    if (m) *m = t->m;
+    if (l) *l = t->l;
+    if (o) *o = t->o;
+    return ok();
+}
+
+void pd_tiled_paged_strides(const pd_tiled *t, int64_t s[3]) {
+    if (!t || !s) return;
+    const pd_tiled_dims &d = t->dims;
+    s[0] = static_cast<int64_t>(d.block_size) * d.num_kv_heads * d.head_dim;
+    s[1] = static_cast<int64_t>(d.num_kv_heads) * d.head_dim;
+    s[2] = d.head_dim;
+}
+
+void pd_tiled_scratch_pool_strides(const pd_tiled *t, int64_t s[3]) {
+    if (!t || !s) return;
+    const pd_tiled_dims &d = t->dims;
+    const int64_t stripe = static_cast<int64_t>(d.num_kv_heads) * d.block_size * d.head_dim;
+    s[0] = 2 * stripe;
+    s[1] = d.head_dim;
+    s[2] = static_cast<int64_t>(d.block_size) * d.head_dim;
+}
+
+int pd_tiled_begin(pd_tiled *t, int num_seqs, void *stream) {
+    if (!t) return fail(PD_ERR_INVALID, "null handle");
+    if (num_seqs < 0) return fail(PD_ERR_INVALID, "num_seqs %d < 0", num_seqs);
+    if (num_seqs > t->dims.max_seqs)
+        return fail(PD_ERR_CAPACITY, "begin_step num_seqs %d > max_seqs %d", num_seqs, t->dims.max_seqs);
+    cudaError_t e = pd::launch_tiled_begin(t->m, t->l, t->o, num_seqs * t->dims.num_q_heads,
+                                           t->dims.head_dim, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tiled begin launch");
+    return ok();
+}
+
+// Block extent of a tiled K/V view: the tiled interface passes no pool size,
+// so block ids are bounded by this constant (ids outside read zeros and raise
+// PD_DEV_BAD_BLOCK_ID).
+constexpr long long kTiledBlockExtent = 1LL << 24;
+
+int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_pool,
+                  const int32_t *tile_blocks, const int32_t *tile_block_counts, int num_seqs,
+                  int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                  int last_block_valid_slots, void *stream) {
+    if (!t) return fail(PD_ERR_INVALID, "null handle");
+    if (num_seqs < 0) return fail(PD_ERR_INVALID, "num_seqs %d < 0", num_seqs);
+    if (num_seqs > t->dims.max_seqs)
+        return fail(PD_ERR_CAPACITY, "step_tile num_seqs %d > max_seqs %d", num_seqs, t->dims.max_seqs);
+    if (num_seqs == 0 || t->dims.tile_capacity == 0) return ok();
+    if (!q || !k_pool || !v_pool || !tile_blocks || !tile_block_counts)
+        return fail(PD_ERR_INVALID, "null pointer");
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return fail(PD_ERR_INVALID, "q, k_pool and v_pool must be 16-byte aligned");
+    if (blk_stride <= 0 || tok_stride <= 0 || kvh_stride <= 0 || blk_stride % 8 || tok_stride % 8 ||
+        kvh_stride % 8)
+        return fail(PD_ERR_INVALID,
+                    "strides (blk %lld, tok %lld, kvh %lld) must be positive multiples of 8 elements",
+                    static_cast<long long>(blk_stride), static_cast<long long>(tok_stride),
+                    static_cast<long long>(kvh_stride));
+    const pd_tiled_dims &d = t->dims;
+    const int G = d.num_q_heads / d.num_kv_heads;
+    const int dpad = dpad_for(d.head_dim);
+    const int gn = G <= 8 ? 1 : 2;
+    const int rows = 8 * gn;
+    const int qtiles = (G + rows - 1) / rows;
+    int cluster = 1;
+    if (g_debug_cluster > 0) cluster = g_debug_cluster;
+    const int stages = default_stages(dpad);
+    const long long grid = static_cast<long long>(num_seqs) * d.num_kv_heads * qtiles * cluster;
+    if (grid > 0x7fffffffLL) return fail(PD_ERR_INVALID, "launch too large");
+
+    int err = PD_OK;
+    unsigned int *status = status_ptr(&err);
+    if (!status) return err;
+    CUtensorMap tk, tv;
+    int tok_dim = 1;
+    int rc = encode_kv_map(&tk, &tok_dim, k_pool, d.head_dim, d.block_size, d.num_kv_heads,
+                           kTiledBlockExtent, blk_stride, tok_stride, kvh_stride);
+    if (rc != PD_OK) return rc;
+    rc = encode_kv_map(&tv, &tok_dim, v_pool, d.head_dim, d.block_size, d.num_kv_heads,
+                       kTiledBlockExtent, blk_stride, tok_stride, kvh_stride);
+    if (rc != PD_OK) return rc;
+
+    pd::UnitParams p = {};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.num_blocks = static_cast<int>(kTiledBlockExtent);
+    p.tile_blocks = tile_blocks;
+    p.tile_counts = tile_block_counts;
+    p.tile_capacity = d.tile_capacity;
+    p.last_valid = last_block_valid_slots;
+    p.st_m = t->m;
+    p.st_l = t->l;
+    p.st_o = t->o;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = d.num_q_heads;
+    p.num_kv_heads = d.num_kv_heads;
+    p.group = G;
+    p.head_dim = d.head_dim;
+    p.block_size = d.block_size;
+    p.qtiles = qtiles;
+    p.cluster = cluster;
+    p.stages = stages;
+    p.tok_dim = tok_dim;
+    // step_tile carries no scale: 1/sqrt(head_dim), rounded to FP32 first.
+    const float inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.head_dim)));
+    p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
+    p.status = status;
+    const int smem = pd::unit_smem_bytes(dpad, rows, stages);
+    cudaError_t e = dispatch_unit<pd::kModeTiled>(dpad, gn, false, tk, tv, p, static_cast<int>(grid),
+                                                  smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tiled step launch");
+    return ok();
+}
+
+int pd_tiled_finalize(pd_tiled *t, void *out, int num_seqs, void *stream) {
+    if (!t) return fail(PD_ERR_INVALID, "null handle");
+    if (num_seqs < 0) return fail(PD_ERR_INVALID, "num_seqs %d < 0", num_seqs);
+    if (num_seqs > t->dims.max_seqs)
+        return fail(PD_ERR_CAPACITY, "finalize num_seqs %d > max_seqs %d", num_seqs, t->dims.max_seqs);
+    if (num_seqs == 0) return ok();
+    if (!out) return fail(PD_ERR_INVALID, "null out");
+    cudaError_t e = pd::launch_tiled_finalize(t->l, t->o, static_cast<__nv_bfloat16 *>(out),
+                                              num_seqs * t->dims.num_q_heads, t->dims.head_dim,
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tiled finalize launch");
+    return ok();
+}
+
+// ---- diagnostics ------------------------------------------------------------------------------
+
+int pd_device_status(int *flags) {
+    if (!flags) return fail(PD_ERR_INVALID, "null flags");
+    int err = PD_OK;
+    unsigned int *sp = status_ptr(&err);
+    if (!sp) return err;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned int v = 0;
+    e = cudaMemcpy(&v, sp, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read status");
+    const unsigned int zero = 0;
+    e = cudaMemcpy(sp, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    *flags = static_cast<int>(v);
+    return ok();
+}
+
+void pd_debug_fail_next_allocs(int count) { g_fail_allocs.store(count < 0 ? 0 : count); }
+
+// Launch-shape override for tuning experiments (0 keeps the built-in choice).
+// Stages change only timing; a cluster size other than the built-in one
+// changes the summation order, hence the output bits.
+void pd_debug_set_launch(int stages_per_warp, int cluster) {
+    g_debug_stages = stages_per_warp > 0 && stages_per_warp <= pd::kMaxStagesPerWarp ? stages_per_warp : 0;
+    g_debug_cluster = cluster > 0 && cluster <= pd::kMaxCluster ? cluster : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// pd_internal.h -- declarations shared by the host side (pd_api.cu) and the
+// kernel translation units of libpd.  Not installed; the public ABI is pd.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pd {
+
+// Warps of a unit CTA.  Each warp folds every kWarps-th 16-token tile of the
+// CTA's range; the warps' states are then merged in warp order.  It is part of
+// the arithmetic (it fixes the summation order), so it is a build constant.
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTileTokens = 16;   // tokens per mma tile (the K/V stage)
+constexpr int kBoxCols = 64;      // BF16 columns per TMA box (128 bytes, 128B swizzle)
+constexpr int kMaxStagesPerWarp = 8;
+constexpr int kMaxCluster = 8;
+
+// Tokens per split (module description of attn_splitk: the split size is
+// floored at PD_MIN_KV_PER_SPLIT from the sequence's own length), rounded up
+// to whole cache blocks.  Shared by the host ABI and every kernel so that the
+// split geometry is one function of (context_len, num_splits, block_size).
+__host__ __device__ inline int split_chunk_tokens(int context_len, int num_splits, int block_size,
+                                                  int min_kv_per_split) {
+    int per = context_len > 0 ? (context_len + num_splits - 1) / num_splits : 0;
+    int c = per > min_kv_per_split ? per : min_kv_per_split;
+    return (c + block_size - 1) / block_size * block_size;
+}
+
+__host__ __device__ inline int splits_used(int context_len, int chunk) {
+    return context_len > 0 ? (context_len + chunk - 1) / chunk : 0;
+}
+
+enum UnitMode : int {
+    kModePaged = 0,  // pd_decode_attn: block_table gather, split ranges, out / workspace
+    kModeTiled = 1,  // pd_tiled_step: tile list, fold into the running state
+};
+
+// Everything a unit kernel reads besides the two tensor maps.
+struct UnitParams {
+    const __nv_bfloat16 *q;  // [S, Hq, D]
+    // paged mode
+    const int32_t *block_table;  // [S, max_blocks_per_seq]
+    const int32_t *context_lens; // [S]
+    int max_blocks_per_seq;
+    int num_blocks;
+    int num_splits;
+    int min_kv_per_split;
+    // tiled mode
+    const int32_t *tile_blocks;  // [S, tile_capacity]
+    const int32_t *tile_counts;  // [S]
+    int tile_capacity;
+    int last_valid;
+    // outputs
+    __nv_bfloat16 *out;  // [S, Hq, D]
+    float *ws_o;         // [S, Hq, N, D]   unnormalised o of each split
+    float *ws_ml;        // [S, Hq, N, 2]   (m, l) of each split, m in log2 units
+    float *st_m;         // tiled running state [max_seqs, Hq] (log2 units)
+    float *st_l;
+    float *st_o;         // [max_seqs, Hq, D]
+    // shape
+    int num_seqs, num_q_heads, num_kv_heads, group, head_dim, block_size;
+    int qtiles;       // CTAs per (s, kvh): ceil(group / rows per CTA)
+    int cluster;      // CTAs per unit (thread-block cluster size)
+    int stages;       // pipeline stages per warp
+    int tok_dim;      // tensor-map dimension of the token coordinate (1 or 2)
+    float scale_log2; // softmax scale * log2(e)
+    unsigned int *status;  // device status word (PD_DEV_* flags)
+};
+
+struct MergeParams {
+    const int32_t *context_lens;
+    const float *ws_o;
+    const float *ws_ml;
+    __nv_bfloat16 *out;
+    int num_seqs, num_q_heads, head_dim, num_splits, block_size, min_kv_per_split;
+    int max_tokens;  // max_blocks_per_seq * block_size (context lengths are clamped to it)
+};
+
+// Dynamic shared memory a unit CTA needs.
+int unit_smem_bytes(int dpad, int rows, int stages);
+
+// Kernel launchers (defined in the per-head-dim translation units).
+template <int DPAD, int GN, int MODE, bool PACKED>
+cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p,
+                        int grid_x, int smem_bytes, cudaStream_t stream);
+
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream, bool programmatic);
+cudaError_t launch_tiled_begin(float *m, float *l, float *o, int rows, int head_dim,
+                               cudaStream_t stream);
+cudaError_t launch_tiled_finalize(const float *l, const float *o, __nv_bfloat16 *out, int rows,
+                                  int head_dim, cudaStream_t stream);
+
+// Compile-time values the packed kernel is instantiated with (the kernels'
+// own copy of the pack width and head dim, checked against pd.h).
+int kernel_pack_width();
+int kernel_pack_head_dim();
+
+}  // namespace pd

@@ -1,0 +1,126 @@
+// pd_small.cu -- the light kernels of libpd: the split-K merge pass and the
+// tiled begin / finalize passes.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "pd_device.cuh"
+#include "pd_internal.h"
+
+namespace pd {
+
+namespace {
+
+constexpr int kMergeWarps = 8;
+
+// Merge pass (Module attn_splitk page: the split-K workspace of [o, m, l]
+// slots and the non-associative merge).  One warp per (sequence, q head):
+//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  O = sum_i o_i 2^(m_i - M),
+//   out = O / L as BF16 (0 when L is 0), summed in split order.
+// Sequences with at most one non-empty split were written by the partial
+// pass directly and are skipped here.
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_constant__ MergeParams p) {
+    const float kNegInf = -__int_as_float(0x7f800000);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
+    if (row >= static_cast<long long>(p.num_seqs) * p.num_q_heads) return;
+    const int s = static_cast<int>(row / p.num_q_heads);
+    int L = p.context_lens[s];
+    L = L < 0 ? 0 : (L > p.max_tokens ? p.max_tokens : L);
+    const int chunk = split_chunk_tokens(L, p.num_splits, p.block_size, p.min_kv_per_split);
+    const int nsu = splits_used(L, chunk);
+    if (nsu <= 1) return;
+    dev::griddep_wait();  // the partial pass's workspace is complete and visible
+
+    const float *ml = p.ws_ml + row * p.num_splits * 2;
+    float M = kNegInf;
+    for (int i = 0; i < nsu; ++i) M = fmaxf(M, ml[2 * i]);
+    const int D = p.head_dim;
+    for (int d0 = lane * 4; d0 < D; d0 += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float Lsum = 0.f;
+        for (int i = 0; i < nsu; ++i) {
+            const float mi = ml[2 * i];
+            const float w = mi == kNegInf ? 0.f : dev::exp2_approx(mi - M);
+            Lsum += w * ml[2 * i + 1];
+            const float4 v = *reinterpret_cast<const float4 *>(p.ws_o + (row * p.num_splits + i) * D + d0);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        const bool pos = Lsum > 0.f;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(pos ? __fdiv_rn(acc.x, Lsum) : 0.f,
+                                                  pos ? __fdiv_rn(acc.y, Lsum) : 0.f);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(pos ? __fdiv_rn(acc.z, Lsum) : 0.f,
+                                                  pos ? __fdiv_rn(acc.w, Lsum) : 0.f);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t *>(&lo);
+        pk.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(p.out + row * D + d0) = pk;
+    }
+}
+
+// TiledAttention::begin_step: (m, l, o) <- (-inf, 0, 0) over `rows` rows.
+__global__ void tiled_begin_kernel(float *m, float *l, float *o, long long rows, long long n_o) {
+    const float kNegInf = -__int_as_float(0x7f800000);
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n_o;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        o[i] = 0.f;
+        if (i < rows) {
+            m[i] = kNegInf;
+            l[i] = 0.f;
+        }
+    }
+}
+
+// TiledAttention::finalize: out = o / l as BF16, 0 where l is 0.
+__global__ void tiled_finalize_kernel(const float *l, const float *o, __nv_bfloat16 *out,
+                                      long long n, int head_dim) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float lv = l[i / head_dim];
+        out[i] = __float2bfloat16_rn(lv > 0.f ? __fdiv_rn(o[i], lv) : 0.f);
+    }
+}
+
+int grid_for(long long n, int threads) {
+    long long g = (n + threads - 1) / threads;
+    if (g > 152 * 32) g = 152 * 32;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream, bool programmatic) {
+    const long long rows = static_cast<long long>(p.num_seqs) * p.num_q_heads;
+    if (rows == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps));
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
+}
+
+cudaError_t launch_tiled_begin(float *m, float *l, float *o, int rows, int head_dim,
+                               cudaStream_t stream) {
+    const long long n_o = static_cast<long long>(rows) * head_dim;
+    if (n_o == 0) return cudaSuccess;
+    tiled_begin_kernel<<<grid_for(n_o, 256), 256, 0, stream>>>(m, l, o, rows, n_o);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tiled_finalize(const float *l, const float *o, __nv_bfloat16 *out, int rows,
+                                  int head_dim, cudaStream_t stream) {
+    const long long n = static_cast<long long>(rows) * head_dim;
+    if (n == 0) return cudaSuccess;
+    tiled_finalize_kernel<<<grid_for(n, 256), 256, 0, stream>>>(l, o, out, n, head_dim);
+    return cudaGetLastError();
+}
+
+}  // namespace pd

@@ -1,0 +1,16 @@
+// pd_unit_d256.cu -- unit kernels for head dims padded to 256 columns.
+#include "pd_unit_launch.cuh"
+
+PD_INSTANTIATE_UNIT(256, 1, pd::kModePaged, false)
+PD_INSTANTIATE_UNIT(256, 2, pd::kModePaged, false)
+PD_INSTANTIATE_UNIT(256, 1, pd::kModeTiled, false)
+PD_INSTANTIATE_UNIT(256, 2, pd::kModeTiled, false)
+
+// The GQA-packed pass: group width PD_GQA at head dim PD_HDIM, compile-time.
+PD_INSTANTIATE_UNIT(PD_HDIM, 1, pd::kModePaged, true)
+
+namespace pd {
+int kernel_pack_width() { return PD_GQA; }
+int kernel_pack_head_dim() { return PD_HDIM; }
+int unit_smem_bytes(int dpad, int rows, int stages) { return unit_smem_plan(dpad, rows, stages).total; }
+}  // namespace pd

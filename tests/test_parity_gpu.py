@@ -1,0 +1,157 @@
+"""GPU parity: libpd (through the C ABI) against the FP64 oracle, element by
+element, within |gpu - ref| <= ulp_bf16(ref) + 1e-3.
+
+Covers the five workloads at full size (the large-batch one on sampled
+sequences, since the oracle is slow there), every split count on the tiny
+workload, ragged and edge-case shapes (empty sequences, 1-token sequences,
+partial last tiles, head dims that are not multiples of 64, group widths from
+1 to 32, block sizes 16/32/64) and both tiled layouts."""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import policy as P
+from paged_kv_decode_splitk_gb300 import api, pd
+from paged_kv_decode_splitk_gb300 import workloads as W
+
+from helpers import assert_within_tolerance, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, device, num_splits=None, gqa_pack=None):
+    inp = api.PagedInputs(w, device)
+    out = api.run_paged(inp, num_splits=num_splits, gqa_pack=gqa_pack)
+    assert out is not None
+    assert pd.pd_device_status() == 0
+    return api.bf16_to_f64(out)
+
+
+@pytest.mark.parametrize("pin", [1, 3])
+def test_tiny_pinned_1_and_3(cuda_device, pin):
+    w = W.tiny(pin=pin)
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    assert_within_tolerance(_run(w, cuda_device, num_splits=pin), ref, f"tiny N={pin}")
+
+
+def test_tiny_every_split_count(cuda_device):
+    w = W.tiny()
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    for n in list(range(1, 17)) + [40, 148]:
+        assert_within_tolerance(_run(w, cuda_device, num_splits=n), ref, f"tiny N={n}")
+
+
+EDGE_SHAPES = [
+    # lens, Hq, Hkv, D, bs, N
+    ([0, 1, 15, 16, 17, 31, 33, 255, 256, 257, 1000], 8, 2, 128, 16, 1),
+    ([0, 1, 15, 16, 17, 31, 33, 255, 256, 257, 1000], 8, 2, 128, 16, 5),
+    ([1, 7, 300, 2000], 4, 4, 64, 16, 3),        # MHA (group 1)
+    ([5, 600, 1200], 12, 4, 128, 16, 2),         # group 3
+    ([17, 513, 3000], 24, 8, 128, 16, 13),
+    ([40, 700], 16, 1, 256, 16, 4),              # group 16 (two 8-row halves)
+    ([40, 700], 32, 1, 64, 16, 2),               # group 32 (two CTAs per KV head)
+    ([90, 333], 12, 1, 96, 16, 3),               # head dim padded 96 -> 128
+    ([90, 333], 4, 2, 8, 16, 2),                 # head dim 8
+    ([90, 333], 8, 2, 160, 16, 1),               # head dim padded 160 -> 256
+    ([77, 500, 1025], 8, 1, 128, 32, 3),         # block size 32
+    ([77, 500, 1025], 8, 2, 128, 64, 4),         # block size 64
+    ([0, 0, 0], 8, 2, 128, 16, 3),               # nothing at all
+]
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,D,bs,N", EDGE_SHAPES)
+def test_edge_shapes(cuda_device, lens, Hq, Hkv, D, bs, N):
+    w = W.custom(lens, Hq, Hkv, D, block_size=bs, seed=31)
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    got = _run(w, cuda_device, num_splits=N, gqa_pack=False)
+    assert_within_tolerance(got, ref, f"{lens} Hq{Hq} Hkv{Hkv} D{D} bs{bs} N{N}")
+    for s, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[s] == 0.0)
+
+
+def test_gqa_packed_full_size(cuda_device):
+    w = W.gqa_packed()
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    assert_within_tolerance(_run(w, cuda_device, num_splits=1, gqa_pack=True), ref, "gqa_packed")
+
+
+def test_gqa_packed_ragged_and_empty(cuda_device):
+    w = W.custom([0, 1, 16, 17, 250, 4097], 16, 2, 256, seed=32)
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    got = _run(w, cuda_device, num_splits=1, gqa_pack=True)
+    assert_within_tolerance(got, ref, "packed ragged")
+    assert np.all(got[0] == 0.0)
+
+
+def test_gqa_pack_not_applicable_launches_nothing(cuda_device):
+    import torch
+    w = W.custom([50], 8, 2, 256, seed=33)  # group 4: not the packed shape
+    inp = api.PagedInputs(w, cuda_device)
+    out = torch.full((1, 8, 256), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    rc = pd.pd_decode_attn(inp.q, inp.k, inp.v, inp.block_table, inp.context_lens, out, w.inv_sqrt_d,
+                           1, None, True)
+    assert rc == pd.PD_NOT_APPLICABLE
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
+
+
+def test_long_context_full_size(cuda_device):
+    w = W.long_context()
+    n = pd.pd_num_splits("auto", 0, 148, w.num_q_heads, 1, 0)
+    assert n == 13
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    assert_within_tolerance(_run(w, cuda_device, num_splits=n), ref, "long_context")
+
+
+def test_large_batch_full_size_sampled(cuda_device):
+    w = W.large_batch()
+    n = pd.pd_num_splits("auto", 0, 148, w.num_q_heads, w.num_seqs, 0)
+    assert n == 10
+    got = _run(w, cuda_device, num_splits=n)
+    lens = w.context_lens
+    rng = np.random.default_rng(7)
+    pick = sorted(set([int(np.argmax(lens)), int(np.argmin(lens)), 0, w.num_seqs - 1]
+                      + list(rng.choice(w.num_seqs, 8, replace=False))))
+    ref = oracle_rows(w, pick)
+    assert_within_tolerance(got[pick], ref, "large_batch sample")
+
+
+def _tiled_check(tw, device, what):
+    inp = api.TiledInputs(tw, device)
+    got = api.bf16_to_f64(api.run_tiled(inp))
+    assert pd.pd_device_status() == 0
+    if tw.layout == "scratch":
+        kf, vf = W.scratch_pool_views(tw.pool)
+        strides = oracle.scratch_pool_strides(tw.num_kv_heads, tw.head_dim, tw.block_size)
+    else:
+        kf, vf = tw.pool, tw.v_pool
+        strides = oracle.paged_strides(tw.num_kv_heads, tw.head_dim, tw.block_size)
+    ref = oracle.tiled_attn(tw.q, kf, vf, tw.tile_blocks, tw.tile_block_counts,
+                            tw.last_block_valid_slots, tw.num_kv_heads, tw.block_size, strides)
+    assert_within_tolerance(got, ref, what)
+    zero = np.where(tw.tile_block_counts.sum(axis=0) == 0)[0]
+    assert len(zero) >= 1
+    assert np.all(got[zero] == 0.0)
+
+
+def test_tiled_scratch_pool_full_size(cuda_device):
+    _tiled_check(W.tiled(), cuda_device, "tiled scratch")
+
+
+def test_tiled_paged_layout(cuda_device):
+    _tiled_check(W.tiled(num_seqs=16, layout="paged", max_blocks=150), cuda_device, "tiled paged")
+
+
+@pytest.mark.parametrize("G,D", [(1, 64), (3, 128), (8, 128), (16, 64)])
+def test_tiled_other_groups(cuda_device, G, D):
+    tw = W.tiled(num_seqs=9, num_q_heads=2 * G, num_kv_heads=2, head_dim=D, tile_capacity=8,
+                 num_calls=3, max_blocks=24, last_valid=11, seed=5)
+    _tiled_check(tw, cuda_device, f"tiled G{G} D{D}")
+
+
+def test_split_geometry_matches_oracle_policy():
+    for L in (0, 1, 255, 256, 257, 32768):
+        for n in (1, 3, 13):
+            assert pd.pd_split_chunk_tokens(L, n, 16) == P.split_chunk_tokens(L, n, 16)
