@@ -38,7 +38,24 @@ int ok() {
 }
 
 int cuda_fail(cudaError_t e, const char *what) {
+    (void)cudaGetLastError();  // reported here: do not leave it for the next launch check
     return fail(PD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Largest dynamic shared memory a block may opt in to on the current device.
+int max_smem_optin() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            (void)cudaGetLastError();
+        cached[dev] = v;
+    }
+    return cached[dev];
 }
 
 // ---- text -----------------------------------------------------------------------
@@ -106,9 +123,62 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 // and KV-head axes in increasing stride order, then the block axis.  Box: 64
 // columns x 16 tokens x 1 head x 1 block, 128-byte swizzle; out-of-range
 // coordinates read zeros.  *tok_dim receives the dimension holding tokens.
+// Encoded maps are cached by their full description (a map depends on nothing
+// else), so repeated launches over the same cache skip the host-side encode.
+struct KvMapKey {
+    const void *base;
+    int head_dim, block_size, num_kv_heads;
+    long long num_blocks, blk_stride, tok_stride, kvh_stride;
+    bool operator==(const KvMapKey &o) const {
+        return base == o.base && head_dim == o.head_dim && block_size == o.block_size &&
+               num_kv_heads == o.num_kv_heads && num_blocks == o.num_blocks &&
+               blk_stride == o.blk_stride && tok_stride == o.tok_stride && kvh_stride == o.kvh_stride;
+    }
+};
+struct KvMapEntry {
+    KvMapKey key;
+    CUtensorMap map;
+    int tok_dim;
+    unsigned long long stamp;
+};
+constexpr int kMapCache = 32;
+std::mutex g_map_mu;
+KvMapEntry g_maps[kMapCache];
+unsigned long long g_map_clock = 0;
+
+int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int head_dim,
+                           int block_size, int num_kv_heads, long long num_blocks,
+                           long long blk_stride, long long tok_stride, long long kvh_stride);
+
 int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim, int block_size,
                   int num_kv_heads, long long num_blocks, long long blk_stride, long long tok_stride,
                   long long kvh_stride) {
+    const KvMapKey key = {base, head_dim, block_size, num_kv_heads, num_blocks, blk_stride, tok_stride,
+                          kvh_stride};
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    int victim = 0;
+    for (int i = 0; i < kMapCache; ++i) {
+        if (g_maps[i].stamp != 0 && g_maps[i].key == key) {
+            g_maps[i].stamp = ++g_map_clock;
+            *map = g_maps[i].map;
+            *tok_dim = g_maps[i].tok_dim;
+            return PD_OK;
+        }
+        if (g_maps[i].stamp < g_maps[victim].stamp) victim = i;
+    }
+    int rc = encode_kv_map_uncached(map, tok_dim, base, head_dim, block_size, num_kv_heads, num_blocks,
+                                    blk_stride, tok_stride, kvh_stride);
+    if (rc != PD_OK) return rc;
+    g_maps[victim].key = key;
+    g_maps[victim].map = *map;
+    g_maps[victim].tok_dim = *tok_dim;
+    g_maps[victim].stamp = ++g_map_clock;
+    return PD_OK;
+}
+
+int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int head_dim,
+                           int block_size, int num_kv_heads, long long num_blocks,
+                           long long blk_stride, long long tok_stride, long long kvh_stride) {
     auto enc = encoder();
     if (!enc) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled entry point");
     const bool tok_first = tok_stride <= kvh_stride;
@@ -153,14 +223,25 @@ int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim
 // so that two or three CTAs share an SM.
 int g_debug_stages = 0;
 int g_debug_cluster = 0;
+int g_debug_prefetch = -1;
+int g_debug_lpt = -1;
 
 int default_stages(int dpad) {
     if (g_debug_stages > 0) return g_debug_stages;
     switch (dpad) {
-        case 64: return 6;
-        case 128: return 3;
+        case 64: return 2;
         default: return 1;
     }
+}
+
+// Tiles each warp prefetches into L2 (TMA prefetch) ahead of its shared-memory
+// ring: deepens the memory pipeline without shared memory.
+int default_prefetch() { return g_debug_prefetch >= 0 ? g_debug_prefetch : 2; }
+
+// Longest-first service order for small batches (a scheduling choice only).
+int default_lpt(int num_seqs) {
+    const int on = g_debug_lpt >= 0 ? g_debug_lpt : 1;
+    return on && num_seqs <= pd::kLptMaxSeqs ? 1 : 0;
 }
 
 // CTAs per packed unit: the packed pass has only num_kv_heads * num_seqs
@@ -171,17 +252,22 @@ constexpr int kPackCluster = 4;
 int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
 
 template <int MODE>
-cudaError_t dispatch_unit(int dpad, int gn, bool packed, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const pd::UnitParams &p, int grid_x, int smem, cudaStream_t st) {
-    if (packed) return pd::launch_unit<256, 1, pd::kModePaged, true>(tk, tv, p, grid_x, smem, st);
-    if (dpad == 64)
-        return gn == 1 ? pd::launch_unit<64, 1, MODE, false>(tk, tv, p, grid_x, smem, st)
-                       : pd::launch_unit<64, 2, MODE, false>(tk, tv, p, grid_x, smem, st);
-    if (dpad == 128)
-        return gn == 1 ? pd::launch_unit<128, 1, MODE, false>(tk, tv, p, grid_x, smem, st)
-                       : pd::launch_unit<128, 2, MODE, false>(tk, tv, p, grid_x, smem, st);
-    return gn == 1 ? pd::launch_unit<256, 1, MODE, false>(tk, tv, p, grid_x, smem, st)
-                   : pd::launch_unit<256, 2, MODE, false>(tk, tv, p, grid_x, smem, st);
+cudaError_t dispatch_unit(int dpad, int gn, bool hl, bool packed, const CUtensorMap &tk,
+                          const CUtensorMap &tv, const pd::UnitParams &p, int grid_x, int smem,
+                          cudaStream_t st) {
+    using namespace pd;
+    if (packed) return launch_unit<256, 1, false, kModePaged, true>(tk, tv, p, grid_x, smem, st);
+#define PD_DISPATCH_D(DP)                                                                   \
+    if (dpad == DP) {                                                                       \
+        if (gn == 2) return launch_unit<DP, 2, false, MODE, false>(tk, tv, p, grid_x, smem, st); \
+        if (hl) return launch_unit<DP, 1, true, MODE, false>(tk, tv, p, grid_x, smem, st);       \
+        return launch_unit<DP, 1, false, MODE, false>(tk, tv, p, grid_x, smem, st);              \
+    }
+    PD_DISPATCH_D(64)
+    PD_DISPATCH_D(128)
+    PD_DISPATCH_D(256)
+#undef PD_DISPATCH_D
+    return cudaErrorInvalidValue;
 }
 
 int check_shape(int num_q_heads, int num_kv_heads, int head_dim, int block_size) {
@@ -463,14 +549,19 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     p.qtiles = qtiles;
     p.cluster = cluster;
     p.stages = stages;
+    p.prefetch = default_prefetch();
+    p.lpt = default_lpt(num_seqs);
     p.tok_dim = tok_dim;
     p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
     p.status = status;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int smem = pd::unit_smem_bytes(dpad, rows, stages);
-    cudaError_t e = dispatch_unit<pd::kModePaged>(dpad, gn, packed, tk, tv, p, static_cast<int>(grid),
-                                                  smem, st);
+    if (smem > max_smem_optin())
+        return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
+                    smem, max_smem_optin());
+    cudaError_t e = dispatch_unit<pd::kModePaged>(dpad, gn, !packed && G <= 4, packed, tk, tv, p,
+                                                  static_cast<int>(grid), smem, st);
     if (e != cudaSuccess) return cuda_fail(e, "unit kernel launch");
     if (num_splits > 1) {
         pd::MergeParams mp = {};
@@ -676,14 +767,20 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     p.qtiles = qtiles;
     p.cluster = cluster;
     p.stages = stages;
+    p.prefetch = default_prefetch();
+    p.lpt = 0;
     p.tok_dim = tok_dim;
     // step_tile carries no scale: 1/sqrt(head_dim), rounded to FP32 first.
     const float inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.head_dim)));
     p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
     p.status = status;
     const int smem = pd::unit_smem_bytes(dpad, rows, stages);
-    cudaError_t e = dispatch_unit<pd::kModeTiled>(dpad, gn, false, tk, tv, p, static_cast<int>(grid),
-                                                  smem, static_cast<cudaStream_t>(stream));
+    if (smem > max_smem_optin())
+        return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
+                    smem, max_smem_optin());
+    cudaError_t e = dispatch_unit<pd::kModeTiled>(dpad, gn, G <= 4, false, tk, tv, p,
+                                                  static_cast<int>(grid), smem,
+                                                  static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tiled step launch");
     return ok();
 }
@@ -723,12 +820,11 @@ int pd_device_status(int *flags) {
 
 void pd_debug_fail_next_allocs(int count) { g_fail_allocs.store(count < 0 ? 0 : count); }
 
-// Launch-shape override for tuning experiments (0 keeps the built-in choice).
-// Stages change only timing; a cluster size other than the built-in one
-// changes the summation order, hence the output bits.
-void pd_debug_set_launch(int stages_per_warp, int cluster) {
+void pd_debug_set_tuning(int stages_per_warp, int cluster, int prefetch, int longest_first) {
     g_debug_stages = stages_per_warp > 0 && stages_per_warp <= pd::kMaxStagesPerWarp ? stages_per_warp : 0;
     g_debug_cluster = cluster > 0 && cluster <= pd::kMaxCluster ? cluster : 0;
+    g_debug_prefetch = prefetch >= 0 && prefetch <= pd::kMaxPrefetch ? prefetch : -1;
+    g_debug_lpt = longest_first == 0 || longest_first == 1 ? longest_first : -1;
 }
 
 }  // extern "C"

@@ -18,6 +18,8 @@ constexpr int kTileTokens = 16;   // tokens per mma tile (the K/V stage)
 constexpr int kBoxCols = 64;      // BF16 columns per TMA box (128 bytes, 128B swizzle)
 constexpr int kMaxStagesPerWarp = 8;
 constexpr int kMaxCluster = 8;
+constexpr int kMaxPrefetch = 8;
+constexpr int kLptMaxSeqs = 64;
 
 // Tokens per split (module description of attn_splitk: the split size is
 // floored at PD_MIN_KV_PER_SPLIT from the sequence's own length), rounded up
@@ -66,6 +68,8 @@ struct UnitParams {
     int qtiles;       // CTAs per (s, kvh): ceil(group / rows per CTA)
     int cluster;      // CTAs per unit (thread-block cluster size)
     int stages;       // pipeline stages per warp
+    int prefetch;     // tiles per warp prefetched into L2 ahead of the stage ring
+    int lpt;          // paged mode: serve sequences longest first (needs num_seqs <= kLptMaxSeqs)
     int tok_dim;      // tensor-map dimension of the token coordinate (1 or 2)
     float scale_log2; // softmax scale * log2(e)
     unsigned int *status;  // device status word (PD_DEV_* flags)
@@ -84,7 +88,7 @@ struct MergeParams {
 int unit_smem_bytes(int dpad, int rows, int stages);
 
 // Kernel launchers (defined in the per-head-dim translation units).
-template <int DPAD, int GN, int MODE, bool PACKED>
+template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
 cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p,
                         int grid_x, int smem_bytes, cudaStream_t stream);
 

@@ -111,16 +111,22 @@ cudaError_t launch_tiled_begin(float *m, float *l, float *o, int rows, int head_
                                cudaStream_t stream) {
     const long long n_o = static_cast<long long>(rows) * head_dim;
     if (n_o == 0) return cudaSuccess;
-    tiled_begin_kernel<<<grid_for(n_o, 256), 256, 0, stream>>>(m, l, o, rows, n_o);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_for(n_o, 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, tiled_begin_kernel, m, l, o, static_cast<long long>(rows), n_o);
 }
 
 cudaError_t launch_tiled_finalize(const float *l, const float *o, __nv_bfloat16 *out, int rows,
                                   int head_dim, cudaStream_t stream) {
     const long long n = static_cast<long long>(rows) * head_dim;
     if (n == 0) return cudaSuccess;
-    tiled_finalize_kernel<<<grid_for(n, 256), 256, 0, stream>>>(l, o, out, n, head_dim);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_for(n, 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, tiled_finalize_kernel, l, o, out, n, head_dim);
 }
 
 }  // namespace pd

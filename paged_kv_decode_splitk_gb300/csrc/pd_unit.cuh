@@ -52,13 +52,17 @@ constexpr unsigned int kDevBadContextLen = 2;
 constexpr unsigned int kDevBadTileCount = 4;
 constexpr unsigned int kDevWaitTimeout = 8;
 
-// Shared-memory plan of a unit CTA (host and device agree on it).
+// Shared-memory plan of a unit CTA (host and device agree on it).  Offsets are
+// from the 1024-byte-aligned base.  The warp-merge area and the CTA result
+// reuse the stage ring once every tile has been consumed.
 struct UnitSmem {
-    int bars;        // offset of the mbarriers (after 1024-byte alignment slack)
-    int stages;      // offset of the stage ring (1024-aligned)
-    int merge;       // per-warp (m, l, o) for the warp merge: overlaps the ring
-    int result;      // CTA result (m, l, o) read by the cluster peers
-    int total;
+    int stages;  // stage ring (offset 0, 1024-aligned)
+    int merge;   // per-warp (o, m, l, weight) for the warp merge: overlaps the ring
+    int result;  // CTA result (o, m, l, m_old, l_old), read by the cluster peers: overlaps the ring
+    int qs;      // the CTA's query rows, BF16, padded rows
+    int bars;    // one mbarrier per stage
+    int lpt;     // longest-first order: context lengths + the pick
+    int total;   // bytes to request, including the alignment slack
 };
 
 __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stages_per_warp) {
@@ -66,19 +70,21 @@ __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stage
     const int stage_bytes = 2 * kTileTokens * dpad * 2;
     const int ring = kWarps * stages_per_warp * stage_bytes;
     const int ostride = dpad + 4;
-    const int merge = kWarps * rows * (ostride + 3) * 4;  // o + m + l + weight
-    s.bars = 0;
-    const int bar_bytes = kWarps * stages_per_warp * 8;
-    s.stages = (bar_bytes + 1023) / 1024 * 1024;
-    s.merge = s.stages;
-    const int big = ring > merge ? ring : merge;
-    s.result = s.stages + (big + 15) / 16 * 16;
-    const int result_bytes = rows * (ostride + 4) * 4;  // o + m + l + m_old + l_old
-    s.total = 1024 /* alignment slack */ + s.result + result_bytes;
+    const int merge = kWarps * rows * (ostride + 3) * 4;
+    const int result = rows * (ostride + 4) * 4;
+    s.stages = 0;
+    s.merge = 0;
+    s.result = (merge + 15) / 16 * 16;
+    int end = s.result + result;
+    if (ring > end) end = ring;
+    s.qs = (end + 15) / 16 * 16;
+    s.bars = s.qs + rows * (dpad * 2 + 16);
+    s.lpt = s.bars + kWarps * stages_per_warp * 8;
+    s.total = 1024 /* alignment slack */ + s.lpt + (kLptMaxSeqs + 4) * 4;
     return s;
 }
 
-template <int DPAD, int GN, int MODE, bool PACKED>
+template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
 __global__ void __launch_bounds__(kThreads)
     unit_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const __grid_constant__ UnitParams p) {
@@ -116,7 +122,31 @@ __global__ void __launch_bounds__(kThreads)
     const int qt = u % p.qtiles;
     u /= p.qtiles;
     const int kvh = u % p.num_kv_heads;
-    const int s = u / p.num_kv_heads;
+    int s = u / p.num_kv_heads;
+    if constexpr (MODE == kModePaged) {
+        if (p.lpt) {
+            // Serve the s-th longest sequence (ties by index), so that the
+            // longest units start first.  Only which CTA serves a sequence
+            // changes; its arithmetic does not.
+            int *lens_s = reinterpret_cast<int *>(smem + plan.lpt);
+            int &pick_s = lens_s[kLptMaxSeqs];
+            const int ns = p.num_seqs;
+            const int Lmax = p.max_blocks_per_seq * p.block_size;
+            for (int c = tid; c < ns; c += kThreads) {
+                const int Lc = p.context_lens[c];
+                lens_s[c] = Lc < 0 ? 0 : (Lc > Lmax ? Lmax : Lc);
+            }
+            __syncthreads();
+            for (int c = tid; c < ns; c += kThreads) {
+                const int Lc = lens_s[c];
+                int rank = 0;
+                for (int j = 0; j < ns; ++j) rank += (lens_s[j] > Lc) || (lens_s[j] == Lc && j < c);
+                if (rank == s) pick_s = c;
+            }
+            __syncthreads();
+            s = pick_s;
+        }
+    }
     const int G = PACKED ? PD_GQA : p.group;
     const int D = PACKED ? PD_HDIM : p.head_dim;
     const int Hq = PACKED ? p.num_kv_heads * PD_GQA : p.num_q_heads;
@@ -215,61 +245,96 @@ __global__ void __launch_bounds__(kThreads)
                              c1, c2, id, policy);
     };
 
+    auto prefetch = [&](int r, int id) {
+        const int gt = my0 + warp + kWarps * r;
+        const int sub = (gt % tiles_per_block) * kTileTokens;
+        const int c1 = p.tok_dim == 1 ? sub : kvh;
+        const int c2 = p.tok_dim == 1 ? kvh : sub;
+#pragma unroll
+        for (int b = 0; b < NBOX; ++b) {
+            dev::tma_prefetch_4d(&tmk, b * kBoxCols, c1, c2, id);
+            dev::tma_prefetch_4d(&tmv, b * kBoxCols, c1, c2, id);
+        }
+    };
+
+    // Block ids of local tiles [32*win, 32*win + 64): lane l of id_cur holds
+    // tile 32*win + l, lane l of id_nxt tile 32*win + 32 + l.
+    int win = 0;
     int id_cur = load_id(lane);
     int id_nxt = load_id(32 + lane);
+    auto id_at = [&](int r) -> int {
+        const int a = __shfl_sync(0xffffffffu, id_cur, r & 31);
+        const int b = __shfl_sync(0xffffffffu, id_nxt, r & 31);
+        return (r >> 5) == win ? a : b;
+    };
+    const int PF = p.prefetch;
     const int npro = nloc < S ? nloc : S;
     for (int r = 0; r < npro; ++r) {
         const int id = __shfl_sync(0xffffffffu, id_cur, r);
         if (lane == 0) issue(r, r, id);
     }
+    for (int r = S; r < S + PF; ++r) {
+        if (r >= nloc) break;
+        const int id = id_at(r);
+        if (lane == 0) prefetch(r, id);
+    }
 
-    // ---- q fragments (A operand of q.K^T), rows past the group are zero -------
-    const int qrow = lane >> 2;        // row within an 8-row half
-    const int qcol = (lane & 3) * 2;   // column pair within a 16-column k-step
-    uint32_t qa[KS][2 * GN];
+    // ---- query rows -> shared memory (rows past the group and columns past
+    // head_dim are zero); A fragments are read back with ldmatrix per k-step.
+    constexpr int QST = DPAD * 2 + 16;  // padded row stride (bytes): conflict-free ldmatrix
+    uint8_t *qsm = smem + plan.qs;
     {
         const __nv_bfloat16 *qb = p.q + (static_cast<long long>(s) * Hq + h0) * D;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-            for (int r = 0; r < GN; ++r) {
-                const int g = qrow + 8 * r;
-#pragma unroll
-                for (int hlf = 0; hlf < 2; ++hlf) {
-                    const int d = ks * 16 + hlf * 8 + qcol;
-                    uint32_t v = 0;
-                    if (g < Gt && d < D)
-                        v = __ldg(reinterpret_cast<const unsigned int *>(qb + static_cast<long long>(g) * D + d));
-                    // A register order: {row g k0-7, row g+8 k0-7, row g k8-15, row g+8 k8-15}
-                    qa[ks][hlf * GN + r] = v;
-                }
-            }
+        for (int e = tid; e < RT * (DPAD / 2); e += kThreads) {
+            const int g = e / (DPAD / 2);
+            const int d = (e - g * (DPAD / 2)) * 2;
+            uint32_t v = 0;
+            if (g < Gt && d < D)
+                v = __ldg(reinterpret_cast<const unsigned int *>(qb + static_cast<long long>(g) * D + d));
+            *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) = v;
         }
     }
+    __syncthreads();
+    // B operand of S^T = K q^T (q^T: d x g), one x2 ldmatrix per k-step and
+    // n-tile: lanes 0-7 address rows g of columns k0..k0+7, lanes 8-15 k0+8..15.
+    const uint32_t q_lm = dev::smem_addr(qsm) + (lane & 7) * QST + ((lane >> 3) & 1) * 16;
 
     // ---- per-lane ldmatrix offsets (128B swizzle: chunk c of row t at c ^ (t & 7)) ----
+    // K as the A operand (t x d): matrices {t 0-7 | 8-15} x {d 0-7 | 8-15}, t fastest.
+    // V^T as the A operand (d x t, via .trans): {t 0-7 | 8-15} slowest, d halves fastest.
     const int lm_j = lane >> 3;
-    const int lm_tok = ((lm_j >> 1) << 3) | (lane & 7);
-    uint32_t lm_off[4];
+    uint32_t lmk_off[4], lmv_off[4];
 #pragma unroll
-    for (int c2 = 0; c2 < 4; ++c2)
-        lm_off[c2] = lm_tok * 128 + ((((2 * c2) + (lm_j & 1)) ^ (lane & 7)) << 4);
+    for (int c2 = 0; c2 < 4; ++c2) {
+        const int tk = ((lm_j & 1) << 3) | (lane & 7);
+        lmk_off[c2] = tk * 128 + ((((2 * c2) + (lm_j >> 1)) ^ (lane & 7)) << 4);
+        const int tv = ((lm_j >> 1) << 3) | (lane & 7);
+        lmv_off[c2] = tv * 128 + ((((2 * c2) + (lm_j & 1)) ^ (lane & 7)) << 4);
+    }
 
     // ---- online-softmax state ---------------------------------------------------
+    // Accumulator layouts (m16n8 fragments): S^T[t][g] with t = lane/4 (+8),
+    // g = nt*8 + (lane%4)*2 (+1); O^T[d][g] with d = mt*16 + lane/4 (+8) and the
+    // same g.  Each thread keeps (m, l) of its two columns g.  With HL (groups of
+    // at most 4) columns 4..7 of the single n-tile carry the BF16 residual of P
+    // for columns 0..3, so one mma per m-tile serves both halves of P.
+    const int tq = lane >> 2;         // token row of the S^T fragment
+    const int gq = (lane & 3) * 2;    // first column (group row) of this thread
     float o[KS][GN][4];
 #pragma unroll
-    for (int a = 0; a < KS; ++a)
+    for (int a_ = 0; a_ < KS; ++a_)
 #pragma unroll
-        for (int b = 0; b < GN; ++b)
+        for (int b_ = 0; b_ < GN; ++b_)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) o[a][b][c] = 0.f;
-    float m_run[GN], l_run[GN];
+            for (int c = 0; c < 4; ++c) o[a_][b_][c] = 0.f;
+    float m_run[GN][2], l_run[GN][2];
 #pragma unroll
-    for (int r = 0; r < GN; ++r) {
-        m_run[r] = kNegInf;
-        l_run[r] = 0.f;
-    }
-    const int tokb = (lane & 3) * 2;  // this lane's token pair within an 8-token n-tile
+    for (int nt = 0; nt < GN; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            m_run[nt][c] = kNegInf;
+            l_run[nt][c] = 0.f;
+        }
     bool aborted = false;
     int fail_r = 0;
 
@@ -287,74 +352,96 @@ __global__ void __launch_bounds__(kThreads)
         const uint32_t kbase = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES);
         const uint32_t vbase = kbase + TILE_BYTES;
 
-        // S = q . K^T  (two n-tiles of 8 tokens)
-        float sc[2][4];
+        // S^T = K . q^T, two accumulator chains (even / odd k-steps)
+        float sc[GN][2][4];
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int nt = 0; nt < GN; ++nt)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) sc[n][c] = 0.f;
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc[nt][h2][c] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            dev::ldsm_x4(kbase + (ks >> 2) * (kTileTokens * 128) + lm_off[ks & 3], b0, b1, b2, b3);
             uint32_t a0, a1, a2, a3;
-            if constexpr (GN == 2) {
-                a0 = qa[ks][0];
-                a1 = qa[ks][1];
-                a2 = qa[ks][2];
-                a3 = qa[ks][3];
-            } else {
-                a0 = qa[ks][0];
-                a1 = 0u;
-                a2 = qa[ks][1];
-                a3 = 0u;
+            dev::ldsm_x4(kbase + (ks >> 2) * (kTileTokens * 128) + lmk_off[ks & 3], a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < GN; ++nt) {
+                uint32_t b0, b1;
+                dev::ldsm_x2(q_lm + nt * 8 * QST + ks * 32, b0, b1);
+                dev::mma_bf16_16816(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
             }
-            dev::mma_bf16_16816(sc[0], a0, a1, a2, a3, b0, b1);
-            dev::mma_bf16_16816(sc[1], a0, a1, a2, a3, b2, b3);
         }
 
-        // scale to base 2, mask tokens past the range, row max
-        float alpha[GN];
-        float pr[GN][2][2];  // [row half][n-tile][token of the pair]
+        // column softmax over the tile's tokens, base 2, tokens past the range masked
+        float alpha[GN][2];
+        float pv[GN][4];
 #pragma unroll
-        for (int r2 = 0; r2 < GN; ++r2) {
-            float mx = kNegInf;
+        for (int nt = 0; nt < GN; ++nt) {
+            float x[4];
 #pragma unroll
-            for (int n = 0; n < 2; ++n)
+            for (int c = 0; c < 4; ++c) {
+                const int t = tq + (c >> 1) * 8;
+                const float v = (sc[nt][0][c] + sc[nt][1][c]) * p.scale_log2;
+                x[c] = t < nvalid ? v : kNegInf;
+            }
+            float cmx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int t = n * 8 + tokb + j;
-                    float x = sc[n][2 * r2 + j] * p.scale_log2;
-                    x = t < nvalid ? x : kNegInf;
-                    pr[r2][n][j] = x;
-                    mx = fmaxf(mx, x);
-                }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run[r2], mx);
-            alpha[r2] = dev::exp2_approx(m_run[r2] - m_new);
-            float sum = 0.f;
+            for (int off = 4; off < 32; off <<= 1) {
+                cmx[0] = fmaxf(cmx[0], __shfl_xor_sync(0xffffffffu, cmx[0], off));
+                cmx[1] = fmaxf(cmx[1], __shfl_xor_sync(0xffffffffu, cmx[1], off));
+            }
 #pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float e = dev::exp2_approx(pr[r2][n][j] - m_new);
-                    pr[r2][n][j] = e;
-                    sum += e;
-                }
-            l_run[r2] = l_run[r2] * alpha[r2] + sum;
-            m_run[r2] = m_new;
+            for (int c = 0; c < 2; ++c) {
+                const float m_new = fmaxf(m_run[nt][c], cmx[c]);
+                alpha[nt][c] = dev::exp2_approx(m_run[nt][c] - m_new);
+                const float e0 = dev::exp2_approx(x[c] - m_new);
+                const float e1 = dev::exp2_approx(x[c + 2] - m_new);
+                pv[nt][c] = e0;
+                pv[nt][c + 2] = e1;
+                l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + (e0 + e1);
+                m_run[nt][c] = m_new;
+            }
         }
 
-        // rescale O^T columns (query rows) whose max moved
+        // P^T as the B operand of O^T += V^T P^T: pack to BF16 (high part and
+        // residual) and transpose each 8x8 block in registers.
+        uint32_t bh[GN][2], bl[GN][2];
+#pragma unroll
+        for (int nt = 0; nt < GN; ++nt)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const float e0 = pv[nt][2 * h2], e1 = pv[nt][2 * h2 + 1];
+                const uint32_t hi = dev::pack_bf16x2(e0, e1);
+                const uint32_t lo = dev::pack_bf16x2(e0 - dev::bf16_lo_f32(hi), e1 - dev::bf16_hi_f32(hi));
+                bh[nt][h2] = dev::movmatrix_trans(hi);
+                bl[nt][h2] = dev::movmatrix_trans(lo);
+            }
+        if constexpr (HL) {
+            // lanes 16..31 hold rows g = 4..7 of the transposed blocks: give them
+            // the residual of rows 0..3 instead
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t lo_src = __shfl_sync(0xffffffffu, bl[0][h2], lane & 15);
+                bh[0][h2] = lane < 16 ? bh[0][h2] : lo_src;
+            }
+        }
+
+        // rescale O^T columns whose max moved (HL: columns 4..7 follow 0..3)
         bool any = false;
 #pragma unroll
-        for (int r2 = 0; r2 < GN; ++r2) any |= alpha[r2] != 1.f;
+        for (int nt = 0; nt < GN; ++nt) any |= (alpha[nt][0] != 1.f) | (alpha[nt][1] != 1.f);
         if (__any_sync(0xffffffffu, any)) {
 #pragma unroll
             for (int nt = 0; nt < GN; ++nt) {
-                const float a0 = __shfl_sync(0xffffffffu, alpha[nt], (lane & 3) * 8);
-                const float a1 = __shfl_sync(0xffffffffu, alpha[nt], (lane & 3) * 8 + 4);
+                float a0 = alpha[nt][0], a1 = alpha[nt][1];
+                if constexpr (HL) {
+                    const float p0 = __shfl_xor_sync(0xffffffffu, a0, 2);
+                    const float p1 = __shfl_xor_sync(0xffffffffu, a1, 2);
+                    if (lane & 2) {
+                        a0 = p0;
+                        a1 = p1;
+                    }
+                }
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     o[mt][nt][0] *= a0;
@@ -365,30 +452,19 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
 
-        // P^T as the B operand: high BF16 part and BF16 residual
-        uint32_t bh[GN][2], bl[GN][2];
-#pragma unroll
-        for (int nt = 0; nt < GN; ++nt)
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                const float e0 = pr[nt][n][0], e1 = pr[nt][n][1];
-                const uint32_t hi = dev::pack_bf16x2(e0, e1);
-                bh[nt][n] = hi;
-                bl[nt][n] = dev::pack_bf16x2(e0 - dev::bf16_lo_f32(hi), e1 - dev::bf16_hi_f32(hi));
-            }
-
         // token masks for a partial tile (V rows past the range may hold anything)
+        const int tv0 = (lane & 3) * 2;
         uint32_t mask01 = 0xffffffffu, mask89 = 0xffffffffu;
         if (nvalid < kTileTokens) {
-            mask01 = (tokb < nvalid ? 0x0000ffffu : 0u) | (tokb + 1 < nvalid ? 0xffff0000u : 0u);
-            mask89 = (tokb + 8 < nvalid ? 0x0000ffffu : 0u) | (tokb + 9 < nvalid ? 0xffff0000u : 0u);
+            mask01 = (tv0 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 1 < nvalid ? 0xffff0000u : 0u);
+            mask89 = (tv0 + 8 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 9 < nvalid ? 0xffff0000u : 0u);
         }
 
         // O^T += V^T . P^T
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
             uint32_t a0, a1, a2, a3;
-            dev::ldsm_x4_trans(vbase + (mt >> 2) * (kTileTokens * 128) + lm_off[mt & 3], a0, a1, a2, a3);
+            dev::ldsm_x4_trans(vbase + (mt >> 2) * (kTileTokens * 128) + lmv_off[mt & 3], a0, a1, a2, a3);
             a0 &= mask01;
             a1 &= mask01;
             a2 &= mask89;
@@ -396,21 +472,27 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int nt = 0; nt < GN; ++nt) {
                 dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                if constexpr (!HL) dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
             }
         }
 
         // refill this stage with the warp's tile r + S
         const int rn = r + S;
         if (rn < nloc) {
-            if ((rn & 31) == 0) {
+            if ((rn >> 5) != win) {
                 id_cur = id_nxt;
-                id_nxt = load_id(rn + 32 + lane);
+                win = rn >> 5;
+                id_nxt = load_id((win + 1) * 32 + lane);
             }
-            const int id = __shfl_sync(0xffffffffu, id_cur, rn & 31);
+            const int id = id_at(rn);
+            const int rp = rn + PF;
+            const int idp = id_at(rp < nloc ? rp : rn);
             dev::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) issue(rn, k, id);
+            if (lane == 0) {
+                issue(rn, k, id);
+                if (PF > 0 && rp < nloc) prefetch(rp, idp);
+            }
         }
     }
     if (aborted) {
@@ -422,22 +504,38 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ---- warp merge (fixed warp order) -------------------------------------------
+    // column sums over the tokens of all lanes of a column
 #pragma unroll
-    for (int r2 = 0; r2 < GN; ++r2) {
-        l_run[r2] += __shfl_xor_sync(0xffffffffu, l_run[r2], 1);
-        l_run[r2] += __shfl_xor_sync(0xffffffffu, l_run[r2], 2);
+    for (int nt = 0; nt < GN; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1)
+                l_run[nt][c] += __shfl_xor_sync(0xffffffffu, l_run[nt][c], off);
+    if constexpr (HL) {
+        // columns 0..3 = high part + residual held in columns 4..7
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) o[mt][0][c] += __shfl_xor_sync(0xffffffffu, o[mt][0][c], 2);
     }
     __syncthreads();  // every warp is done with the ring; reuse it for the merge
     float *wo = reinterpret_cast<float *>(smem + plan.merge);  // [kWarps][RT][OSTRIDE]
     float *wm = wo + kWarps * RT * OSTRIDE;                    // [kWarps][RT]
     float *wl = wm + kWarps * RT;                              // [kWarps][RT]
     float *ww = wl + kWarps * RT;                              // [kWarps][RT] weights
-    if ((lane & 3) == 0) {
+    constexpr int GCOLS = HL ? 4 : 8;  // meaningful columns per n-tile
+    if (tq == 0) {
 #pragma unroll
-        for (int r2 = 0; r2 < GN; ++r2) {
-            wm[warp * RT + qrow + 8 * r2] = m_run[r2];
-            wl[warp * RT + qrow + 8 * r2] = l_run[r2];
-        }
+        for (int nt = 0; nt < GN; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int g = nt * 8 + gq + c;
+                if (g - nt * 8 < GCOLS) {
+                    wm[warp * RT + g] = m_run[nt][c];
+                    wl[warp * RT + g] = l_run[nt][c];
+                }
+            }
     }
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt)
@@ -445,9 +543,9 @@ __global__ void __launch_bounds__(kThreads)
         for (int nt = 0; nt < GN; ++nt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int g = nt * 8 + tokb + (c & 1);
-                const int d = mt * 16 + qrow + (c >> 1) * 8;
-                wo[(warp * RT + g) * OSTRIDE + d] = o[mt][nt][c];
+                const int g = nt * 8 + gq + (c & 1);
+                const int d = mt * 16 + tq + (c >> 1) * 8;
+                if (g - nt * 8 < GCOLS) wo[(warp * RT + g) * OSTRIDE + d] = o[mt][nt][c];
             }
     __syncthreads();
 

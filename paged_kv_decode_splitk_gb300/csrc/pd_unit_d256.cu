@@ -1,13 +1,15 @@
 // pd_unit_d256.cu -- unit kernels for head dims padded to 256 columns.
 #include "pd_unit_launch.cuh"
 
-PD_INSTANTIATE_UNIT(256, 1, pd::kModePaged, false)
-PD_INSTANTIATE_UNIT(256, 2, pd::kModePaged, false)
-PD_INSTANTIATE_UNIT(256, 1, pd::kModeTiled, false)
-PD_INSTANTIATE_UNIT(256, 2, pd::kModeTiled, false)
+PD_INSTANTIATE_UNIT(256, 1, true, pd::kModePaged, false)
+PD_INSTANTIATE_UNIT(256, 1, false, pd::kModePaged, false)
+PD_INSTANTIATE_UNIT(256, 2, false, pd::kModePaged, false)
+PD_INSTANTIATE_UNIT(256, 1, true, pd::kModeTiled, false)
+PD_INSTANTIATE_UNIT(256, 1, false, pd::kModeTiled, false)
+PD_INSTANTIATE_UNIT(256, 2, false, pd::kModeTiled, false)
 
 // The GQA-packed pass: group width PD_GQA at head dim PD_HDIM, compile-time.
-PD_INSTANTIATE_UNIT(PD_HDIM, 1, pd::kModePaged, true)
+PD_INSTANTIATE_UNIT(PD_HDIM, 1, false, pd::kModePaged, true)
 
 namespace pd {
 int kernel_pack_width() { return PD_GQA; }

@@ -10,10 +10,10 @@ namespace pd {
 
 int unit_smem_bytes(int dpad, int rows, int stages);
 
-template <int DPAD, int GN, int MODE, bool PACKED>
+template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
 cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p,
                         int grid_x, int smem_bytes, cudaStream_t stream) {
-    auto kern = unit_kernel<DPAD, GN, MODE, PACKED>;
+    auto kern = unit_kernel<DPAD, GN, HL, MODE, PACKED>;
     // Raise the kernel's dynamic shared-memory limit once per device (and
     // again only if a launch asks for more).
     static std::mutex mu;
@@ -51,6 +51,6 @@ cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const Un
 
 }  // namespace pd
 
-#define PD_INSTANTIATE_UNIT(DPAD, GN, MODE, PACKED)                                          \
-    template cudaError_t pd::launch_unit<DPAD, GN, MODE, PACKED>(                            \
+#define PD_INSTANTIATE_UNIT(DPAD, GN, HL, MODE, PACKED)                                      \
+    template cudaError_t pd::launch_unit<DPAD, GN, HL, MODE, PACKED>(                        \
         const CUtensorMap &, const CUtensorMap &, const pd::UnitParams &, int, int, cudaStream_t);
