@@ -287,13 +287,12 @@ void pd_debug_fail_next_allocs(int count);
 
 /* Tuning hook for launch-shape experiments, applied to the following launches
  * in this process: pipeline stages per warp (1..8; 0 = built-in), CTAs per
- * unit cluster (1..8; 0 = built-in), tiles per warp prefetched into L2 ahead
- * of the stage ring (0..8; -1 = built-in) and longest-first service order of
- * small batches (0/1; -1 = built-in).  Stages, prefetch and order change only
- * timing.  A cluster size other than the built-in one changes the summation
- * order and so the output bits (still within tolerance): never change it
- * between launches whose outputs must be bit-identical. */
-void pd_debug_set_tuning(int stages_per_warp, int cluster, int prefetch, int longest_first);
+ * unit cluster (1..8; 0 = built-in) and longest-first service order of small
+ * batches (0/1; -1 = built-in).  Stages and order change only timing.  A
+ * cluster size other than the built-in one changes the summation order and so
+ * the output bits (still within tolerance): never change it between launches
+ * whose outputs must be bit-identical. */
+void pd_debug_set_tuning(int stages_per_warp, int cluster, int longest_first);
 
 #if defined(__GNUC__)
 #pragma GCC visibility pop

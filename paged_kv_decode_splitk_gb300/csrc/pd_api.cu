@@ -223,7 +223,6 @@ int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int
 // so that two or three CTAs share an SM.
 int g_debug_stages = 0;
 int g_debug_cluster = 0;
-int g_debug_prefetch = -1;
 int g_debug_lpt = -1;
 
 int default_stages(int dpad) {
@@ -234,10 +233,6 @@ int default_stages(int dpad) {
     }
 }
 
-// Tiles each warp prefetches into L2 (TMA prefetch) ahead of its shared-memory
-// ring: deepens the memory pipeline without shared memory.
-int default_prefetch() { return g_debug_prefetch >= 0 ? g_debug_prefetch : 2; }
-
 // Longest-first service order for small batches (a scheduling choice only).
 int default_lpt(int num_seqs) {
     const int on = g_debug_lpt >= 0 ? g_debug_lpt : 1;
@@ -247,7 +242,10 @@ int default_lpt(int num_seqs) {
 // CTAs per packed unit: the packed pass has only num_kv_heads * num_seqs
 // units, so each is spread over a cluster that merges through distributed
 // shared memory.  A build constant (it fixes the summation order).
-constexpr int kPackCluster = 4;
+constexpr int kPackCluster = 6;
+
+// CTAs per tiled unit (same role for step_tile's (sequence, KV head) units).
+constexpr int kTiledCluster = 2;
 
 int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
 
@@ -549,7 +547,6 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     p.qtiles = qtiles;
     p.cluster = cluster;
     p.stages = stages;
-    p.prefetch = default_prefetch();
     p.lpt = default_lpt(num_seqs);
     p.tok_dim = tok_dim;
     p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
@@ -730,7 +727,7 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     const int gn = G <= 8 ? 1 : 2;
     const int rows = 8 * gn;
     const int qtiles = (G + rows - 1) / rows;
-    int cluster = 1;
+    int cluster = kTiledCluster;
     if (g_debug_cluster > 0) cluster = g_debug_cluster;
     const int stages = default_stages(dpad);
     const long long grid = static_cast<long long>(num_seqs) * d.num_kv_heads * qtiles * cluster;
@@ -767,7 +764,6 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     p.qtiles = qtiles;
     p.cluster = cluster;
     p.stages = stages;
-    p.prefetch = default_prefetch();
     p.lpt = 0;
     p.tok_dim = tok_dim;
     // step_tile carries no scale: 1/sqrt(head_dim), rounded to FP32 first.
@@ -820,10 +816,9 @@ int pd_device_status(int *flags) {
 
 void pd_debug_fail_next_allocs(int count) { g_fail_allocs.store(count < 0 ? 0 : count); }
 
-void pd_debug_set_tuning(int stages_per_warp, int cluster, int prefetch, int longest_first) {
+void pd_debug_set_tuning(int stages_per_warp, int cluster, int longest_first) {
     g_debug_stages = stages_per_warp > 0 && stages_per_warp <= pd::kMaxStagesPerWarp ? stages_per_warp : 0;
     g_debug_cluster = cluster > 0 && cluster <= pd::kMaxCluster ? cluster : 0;
-    g_debug_prefetch = prefetch >= 0 && prefetch <= pd::kMaxPrefetch ? prefetch : -1;
     g_debug_lpt = longest_first == 0 || longest_first == 1 ? longest_first : -1;
 }
 

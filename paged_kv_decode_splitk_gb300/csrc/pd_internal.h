@@ -18,7 +18,6 @@ constexpr int kTileTokens = 16;   // tokens per mma tile (the K/V stage)
 constexpr int kBoxCols = 64;      // BF16 columns per TMA box (128 bytes, 128B swizzle)
 constexpr int kMaxStagesPerWarp = 8;
 constexpr int kMaxCluster = 8;
-constexpr int kMaxPrefetch = 8;
 constexpr int kLptMaxSeqs = 64;
 
 // Tokens per split (module description of attn_splitk: the split size is
@@ -68,7 +67,6 @@ struct UnitParams {
     int qtiles;       // CTAs per (s, kvh): ceil(group / rows per CTA)
     int cluster;      // CTAs per unit (thread-block cluster size)
     int stages;       // pipeline stages per warp
-    int prefetch;     // tiles per warp prefetched into L2 ahead of the stage ring
     int lpt;          // paged mode: serve sequences longest first (needs num_seqs <= kLptMaxSeqs)
     int tok_dim;      // tensor-map dimension of the token coordinate (1 or 2)
     float scale_log2; // softmax scale * log2(e)

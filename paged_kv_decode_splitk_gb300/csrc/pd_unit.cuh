@@ -18,14 +18,19 @@
 //     constants, so a sequence's bits never depend on the rest of the batch.
 //   * K and V tiles (16 tokens x head_dim BF16) move global -> shared with 4-D
 //     TMA tensor loads gathered through the block table (one box per 64
-//     columns, 128-byte swizzle), each warp running a private ring of
-//     `stages` mbarrier-tracked buffers that it refills itself.
-//   * q.K^T and P.V run on the tensor cores (mma.sync m16n8k16 BF16 -> FP32):
-//     S[g,t] = q[g,:] K[t,:]^T with q rows as A (rows past the group are zero),
-//     then O^T[d,g] += V^T[d,t] P^T[t,g] with P taken straight from the S
-//     accumulator registers.  P is split into a BF16 high part and a BF16
-//     residual (two mma), which keeps ~16 significant bits of each weight.
-//   * Row max and row sums use warp shuffles across the 4 lanes of a row.
+//     columns, 128-byte swizzle).  Each warp runs a private ring of `stages`
+//     buffers with separate K and V mbarriers: the K half of a buffer is
+//     refilled as soon as q.K^T has read it, the V half after P.V, so the next
+//     tile's loads overlap the current tile's math.
+//   * Both products run on the tensor cores (mma.sync m16n8k16 BF16 -> FP32)
+//     with the tokens as the M dimension: S^T[t,g] = K[t,:] q[g,:]^T (the
+//     group fills N = 8), then O^T[d,g] += V^T[d,t] P^T[t,g].  P^T comes from
+//     the S^T accumulators through an in-register 8x8 transpose (movmatrix).
+//     P is split into a BF16 high part and a BF16 residual, which keeps ~16
+//     significant bits of every weight; for groups of at most 4 the residual
+//     rides in the otherwise idle columns 4..7 of the same mma.
+//   * Column max and column sums of S^T use warp shuffles over the 8 lanes
+//     that hold a column.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -57,29 +62,35 @@ constexpr unsigned int kDevWaitTimeout = 8;
 // reuse the stage ring once every tile has been consumed.
 struct UnitSmem {
     int stages;  // stage ring (offset 0, 1024-aligned)
-    int merge;   // per-warp (o, m, l, weight) for the warp merge: overlaps the ring
-    int result;  // CTA result (o, m, l, m_old, l_old), read by the cluster peers: overlaps the ring
+    int merge;   // per-warp o [kWarps][rows][dpad+4]: overlaps the ring
+    int result;  // CTA result o [rows][dpad+4], read by the cluster peers: overlaps the ring
     int qs;      // the CTA's query rows, BF16, padded rows
-    int bars;    // one mbarrier per stage
+    int stats;   // per-warp m, l, weights; CTA m, l; row factors of the final combine
+    int bars;    // two mbarriers (K, V) per stage
     int lpt;     // longest-first order: context lengths + the pick
     int total;   // bytes to request, including the alignment slack
 };
+
+__host__ __device__ constexpr int unit_stat_floats(int rows) {
+    return rows * (3 * kWarps + 2 + 4 + kMaxCluster);
+}
 
 __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stages_per_warp) {
     UnitSmem s;
     const int stage_bytes = 2 * kTileTokens * dpad * 2;
     const int ring = kWarps * stages_per_warp * stage_bytes;
     const int ostride = dpad + 4;
-    const int merge = kWarps * rows * (ostride + 3) * 4;
-    const int result = rows * (ostride + 4) * 4;
+    const int merge = kWarps * rows * ostride * 4;
+    const int result = rows * ostride * 4;
     s.stages = 0;
     s.merge = 0;
-    s.result = (merge + 15) / 16 * 16;
+    s.result = merge;
     int end = s.result + result;
     if (ring > end) end = ring;
     s.qs = (end + 15) / 16 * 16;
-    s.bars = s.qs + rows * (dpad * 2 + 16);
-    s.lpt = s.bars + kWarps * stages_per_warp * 8;
+    s.stats = s.qs + rows * (dpad * 2 + 16);
+    s.bars = s.stats + (unit_stat_floats(rows) * 4 + 15) / 16 * 16;
+    s.lpt = s.bars + kWarps * stages_per_warp * 2 * 8;
     s.total = 1024 /* alignment slack */ + s.lpt + (kLptMaxSeqs + 4) * 4;
     return s;
 }
@@ -88,27 +99,45 @@ template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
 __global__ void __launch_bounds__(kThreads)
     unit_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const __grid_constant__ UnitParams p) {
-    constexpr int KS = DPAD / 16;      // mma k-steps of q.K^T == m-tiles of V^T.P^T
+    constexpr int KS = DPAD / 16;      // mma k-steps of K.q^T == m-tiles of V^T.P^T
     constexpr int NBOX = DPAD / kBoxCols;
     constexpr int TILE_BYTES = kTileTokens * DPAD * 2;
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     constexpr int RT = 8 * GN;         // query rows per CTA
     constexpr int OSTRIDE = DPAD + 4;  // padded row stride of o in shared memory
+    constexpr int QST = DPAD * 2 + 16; // padded row stride of q in shared memory (bytes)
+    constexpr int QPT = RT * (DPAD / 2) / kThreads;  // q words per thread
+    static_assert(QPT * kThreads == RT * (DPAD / 2), "q staging must divide evenly");
     const float kNegInf = -__int_as_float(0x7f800000);
 
-    if constexpr (MODE == kModePaged) dev::griddep_launch_dependents();
+    // Programmatic dependent launch: let the next kernel in the stream start
+    // its launch now; it waits (griddepcontrol.wait) for this grid to finish
+    // before it touches memory.
+    dev::griddep_launch_dependents();
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int S = p.stages;
     const UnitSmem plan = unit_smem_plan(DPAD, RT, S);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + plan.bars);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + plan.bars);  // [kWarps*S][K, V]
     uint8_t *ring = smem + plan.stages;
+    uint8_t *qsm = smem + plan.qs;
+    float *stats = reinterpret_cast<float *>(smem + plan.stats);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+
+    // Shared-memory set-up needs no global memory: do it before waiting for
+    // the previous kernel in the stream.
+    if (tid == 0) {
+        dev::prefetch_tensormap(&tmk);
+        dev::prefetch_tensormap(&tmv);
+        for (int i = 0; i < 2 * kWarps * S; ++i) dev::mbar_init(dev::smem_addr(&bars[i]), 1);
+        dev::fence_mbar_init();
+    }
+    dev::griddep_wait();  // the previous kernel's writes (q, caches, tables, out) are visible
 
     // ---- which unit ---------------------------------------------------------
     const int C = p.cluster;
@@ -155,6 +184,21 @@ __global__ void __launch_bounds__(kThreads)
     const int Gt = min(RT, G - g0);               // valid rows
     const int h0 = kvh * G + g0;                  // first query head
 
+    // ---- query rows: issue the loads now, they do not depend on the range ----
+    uint32_t qv[QPT];
+    {
+        const __nv_bfloat16 *qb = p.q + (static_cast<long long>(s) * Hq + h0) * D;
+#pragma unroll
+        for (int i = 0; i < QPT; ++i) {
+            const int e = tid + i * kThreads;
+            const int g = e / (DPAD / 2);
+            const int d = (e - g * (DPAD / 2)) * 2;
+            qv[i] = (g < Gt && d < D)
+                        ? __ldg(reinterpret_cast<const unsigned int *>(qb + static_cast<long long>(g) * D + d))
+                        : 0u;
+        }
+    }
+
     // ---- token range of the unit --------------------------------------------
     int tok0 = 0, tok1 = 0;
     bool direct = true;  // paged: write normalised output instead of a partial
@@ -176,9 +220,9 @@ __global__ void __launch_bounds__(kThreads)
         if (tok0 >= tok1) {
             // Empty split.  Split 0 of an empty sequence owns the zero output.
             if (L == 0 && split == 0 && part == 0) {
-                for (int e = tid; e < Gt * D; e += kThreads) {
-                    const int g = e / D, d = e - g * D;
-                    p.out[(static_cast<long long>(s) * Hq + h0 + g) * D + d] = __float2bfloat16_rn(0.f);
+                for (int e = tid; e < Gt * (D / 2); e += kThreads) {
+                    const int g = e / (D / 2), d = (e - g * (D / 2)) * 2;
+                    *reinterpret_cast<uint32_t *>(p.out + (static_cast<long long>(s) * Hq + h0 + g) * D + d) = 0u;
                 }
             }
             return;  // uniform across the cluster: every rank sees the same range
@@ -205,12 +249,13 @@ __global__ void __launch_bounds__(kThreads)
     const int my1 = tile0 + min((part + 1) * per, ntiles);
     const int nloc = my1 - my0 > warp ? (my1 - my0 - warp + kWarps - 1) / kWarps : 0;
 
-    // ---- barriers -------------------------------------------------------------
-    if (tid == 0) {
-        dev::prefetch_tensormap(&tmk);
-        dev::prefetch_tensormap(&tmv);
-        for (int i = 0; i < kWarps * S; ++i) dev::mbar_init(dev::smem_addr(&bars[i]), 1);
-        dev::fence_mbar_init();
+    // ---- q to shared memory (the barriers were initialised at the start) ----------
+#pragma unroll
+    for (int i = 0; i < QPT; ++i) {
+        const int e = tid + i * kThreads;
+        const int g = e / (DPAD / 2);
+        const int d = (e - g * (DPAD / 2)) * 2;
+        *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) = qv[i];
     }
     __syncthreads();
 
@@ -227,34 +272,18 @@ __global__ void __launch_bounds__(kThreads)
         if (id < 0 || id >= p.num_blocks) dev::flag_status(p.status, kDevBadBlockId);
         return id;
     };
-    auto issue = [&](int r, int k, int id) {
+    // TMA of the K (half 0) or V (half 1) tile of local tile r into stage k.
+    auto issue = [&](const CUtensorMap *map, int half, int r, int k, int id) {
         const int gt = my0 + warp + kWarps * r;
         const int sub = (gt % tiles_per_block) * kTileTokens;
-        const uint32_t bar = dev::smem_addr(&bars[warp * S + k]);
-        const uint32_t dst = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES);
+        const uint32_t bar = dev::smem_addr(&bars[(warp * S + k) * 2 + half]);
+        const uint32_t dst = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES + half * TILE_BYTES);
         const int c1 = p.tok_dim == 1 ? sub : kvh;
         const int c2 = p.tok_dim == 1 ? kvh : sub;
-        dev::mbar_arrive_expect_tx(bar, STAGE_BYTES);
+        dev::mbar_arrive_expect_tx(bar, TILE_BYTES);
 #pragma unroll
         for (int b = 0; b < NBOX; ++b)
-            dev::tma_load_4d(dst + b * (kTileTokens * 128), &tmk, bar, b * kBoxCols, c1, c2, id,
-                             policy);
-#pragma unroll
-        for (int b = 0; b < NBOX; ++b)
-            dev::tma_load_4d(dst + TILE_BYTES + b * (kTileTokens * 128), &tmv, bar, b * kBoxCols,
-                             c1, c2, id, policy);
-    };
-
-    auto prefetch = [&](int r, int id) {
-        const int gt = my0 + warp + kWarps * r;
-        const int sub = (gt % tiles_per_block) * kTileTokens;
-        const int c1 = p.tok_dim == 1 ? sub : kvh;
-        const int c2 = p.tok_dim == 1 ? kvh : sub;
-#pragma unroll
-        for (int b = 0; b < NBOX; ++b) {
-            dev::tma_prefetch_4d(&tmk, b * kBoxCols, c1, c2, id);
-            dev::tma_prefetch_4d(&tmv, b * kBoxCols, c1, c2, id);
-        }
+            dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * kBoxCols, c1, c2, id, policy);
     };
 
     // Block ids of local tiles [32*win, 32*win + 64): lane l of id_cur holds
@@ -267,34 +296,15 @@ __global__ void __launch_bounds__(kThreads)
         const int b = __shfl_sync(0xffffffffu, id_nxt, r & 31);
         return (r >> 5) == win ? a : b;
     };
-    const int PF = p.prefetch;
     const int npro = nloc < S ? nloc : S;
     for (int r = 0; r < npro; ++r) {
         const int id = __shfl_sync(0xffffffffu, id_cur, r);
-        if (lane == 0) issue(r, r, id);
-    }
-    for (int r = S; r < S + PF; ++r) {
-        if (r >= nloc) break;
-        const int id = id_at(r);
-        if (lane == 0) prefetch(r, id);
-    }
-
-    // ---- query rows -> shared memory (rows past the group and columns past
-    // head_dim are zero); A fragments are read back with ldmatrix per k-step.
-    constexpr int QST = DPAD * 2 + 16;  // padded row stride (bytes): conflict-free ldmatrix
-    uint8_t *qsm = smem + plan.qs;
-    {
-        const __nv_bfloat16 *qb = p.q + (static_cast<long long>(s) * Hq + h0) * D;
-        for (int e = tid; e < RT * (DPAD / 2); e += kThreads) {
-            const int g = e / (DPAD / 2);
-            const int d = (e - g * (DPAD / 2)) * 2;
-            uint32_t v = 0;
-            if (g < Gt && d < D)
-                v = __ldg(reinterpret_cast<const unsigned int *>(qb + static_cast<long long>(g) * D + d));
-            *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) = v;
+        if (lane == 0) {
+            issue(&tmk, 0, r, r, id);
+            issue(&tmv, 1, r, r, id);
         }
     }
-    __syncthreads();
+
     // B operand of S^T = K q^T (q^T: d x g), one x2 ldmatrix per k-step and
     // n-tile: lanes 0-7 address rows g of columns k0..k0+7, lanes 8-15 k0+8..15.
     const uint32_t q_lm = dev::smem_addr(qsm) + (lane & 7) * QST + ((lane >> 3) & 1) * 16;
@@ -335,15 +345,22 @@ __global__ void __launch_bounds__(kThreads)
             m_run[nt][c] = kNegInf;
             l_run[nt][c] = 0.f;
         }
-    bool aborted = false;
-    int fail_r = 0;
+    int fail_r = -1;
 
     for (int r = 0; r < nloc; ++r) {
         const int k = r % S;
         const uint32_t par = (r / S) & 1;
-        if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[warp * S + k]), par)) {
-            dev::flag_status(p.status, kDevWaitTimeout);
-            aborted = true;
+        const int rn = r + S;
+        int id_next = -1;
+        if (rn < nloc) {
+            if ((rn >> 5) != win) {
+                id_cur = id_nxt;
+                win = rn >> 5;
+                id_nxt = load_id((win + 1) * 32 + lane);
+            }
+            id_next = id_at(rn);
+        }
+        if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 0]), par)) {
             fail_r = r;
             break;
         }
@@ -370,6 +387,12 @@ __global__ void __launch_bounds__(kThreads)
                 dev::ldsm_x2(q_lm + nt * 8 * QST + ks * 32, b0, b1);
                 dev::mma_bf16_16816(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
             }
+        }
+        // the K half is read: refill it with tile r + S
+        if (rn < nloc) {
+            dev::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) issue(&tmk, 0, rn, k, id_next);
         }
 
         // column softmax over the tile's tokens, base 2, tokens past the range masked
@@ -452,55 +475,50 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
 
-        // token masks for a partial tile (V rows past the range may hold anything)
-        const int tv0 = (lane & 3) * 2;
-        uint32_t mask01 = 0xffffffffu, mask89 = 0xffffffffu;
-        if (nvalid < kTileTokens) {
-            mask01 = (tv0 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 1 < nvalid ? 0xffff0000u : 0u);
-            mask89 = (tv0 + 8 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 9 < nvalid ? 0xffff0000u : 0u);
+        if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 1]), par)) {
+            fail_r = r;
+            break;
         }
-
-        // O^T += V^T . P^T
+        // O^T += V^T . P^T  (V rows past the range may hold anything: mask them)
+        auto pv_tile = [&](uint32_t mask01, uint32_t mask89) {
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            dev::ldsm_x4_trans(vbase + (mt >> 2) * (kTileTokens * 128) + lmv_off[mt & 3], a0, a1, a2, a3);
-            a0 &= mask01;
-            a1 &= mask01;
-            a2 &= mask89;
-            a3 &= mask89;
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                dev::ldsm_x4_trans(vbase + (mt >> 2) * (kTileTokens * 128) + lmv_off[mt & 3], a0, a1, a2, a3);
+                a0 &= mask01;
+                a1 &= mask01;
+                a2 &= mask89;
+                a3 &= mask89;
 #pragma unroll
-            for (int nt = 0; nt < GN; ++nt) {
-                dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                if constexpr (!HL) dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                for (int nt = 0; nt < GN; ++nt) {
+                    dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                    if constexpr (!HL) dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                }
             }
+        };
+        if (nvalid == kTileTokens) {
+            pv_tile(0xffffffffu, 0xffffffffu);
+        } else {
+            const int tv0 = (lane & 3) * 2;
+            pv_tile((tv0 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 1 < nvalid ? 0xffff0000u : 0u),
+                    (tv0 + 8 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 9 < nvalid ? 0xffff0000u : 0u));
         }
-
-        // refill this stage with the warp's tile r + S
-        const int rn = r + S;
+        // the V half is read: refill it with tile r + S
         if (rn < nloc) {
-            if ((rn >> 5) != win) {
-                id_cur = id_nxt;
-                win = rn >> 5;
-                id_nxt = load_id((win + 1) * 32 + lane);
-            }
-            const int id = id_at(rn);
-            const int rp = rn + PF;
-            const int idp = id_at(rp < nloc ? rp : rn);
             dev::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                issue(rn, k, id);
-                if (PF > 0 && rp < nloc) prefetch(rp, idp);
-            }
+            if (lane == 0) issue(&tmv, 1, rn, k, id_next);
         }
     }
-    if (aborted) {
-        // Drain whatever this warp still has in flight (bounded) before the
-        // ring is reused, so no copy lands after the CTA moves on.
-        const int last = fail_r + S < nloc ? fail_r + S : nloc;  // tiles issued so far
+    if (fail_r >= 0) {
+        // A bounded wait ran out.  Record it and drain (bounded) whatever this
+        // warp may still have in flight before the ring is reused.
+        if (lane == 0) dev::flag_status(p.status, kDevWaitTimeout);
+        const int last = fail_r + S + 1 < nloc ? fail_r + S + 1 : nloc;
         for (int r = fail_r; r < last; ++r)
-            dev::mbar_wait_bounded(dev::smem_addr(&bars[warp * S + r % S]), (r / S) & 1, 100000000ull);
+            for (int h = 0; h < 2; ++h)
+                dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + r % S) * 2 + h]), (r / S) & 1,
+                                       100000000ull);
     }
 
     // ---- warp merge (fixed warp order) -------------------------------------------
@@ -521,9 +539,13 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();  // every warp is done with the ring; reuse it for the merge
     float *wo = reinterpret_cast<float *>(smem + plan.merge);  // [kWarps][RT][OSTRIDE]
-    float *wm = wo + kWarps * RT * OSTRIDE;                    // [kWarps][RT]
+    float *wm = stats;                                         // [kWarps][RT]
     float *wl = wm + kWarps * RT;                              // [kWarps][RT]
     float *ww = wl + kWarps * RT;                              // [kWarps][RT] weights
+    float *cm = ww + kWarps * RT;                              // [RT] CTA max
+    float *cl = cm + RT;                                       // [RT] CTA sum
+    float *fx = cl + RT;                                       // [RT][4] row factors of the final combine
+    float *fr = fx + 4 * RT;                                   // [RT][kMaxCluster] rank weights
     constexpr int GCOLS = HL ? 4 : 8;  // meaningful columns per n-tile
     if (tq == 0) {
 #pragma unroll
@@ -549,15 +571,13 @@ __global__ void __launch_bounds__(kThreads)
             }
     __syncthreads();
 
-    float *co = reinterpret_cast<float *>(smem + plan.result);  // [RT][OSTRIDE]
-    float *cm = co + RT * OSTRIDE;                               // [RT]
-    float *cl = cm + RT;
-    float *xm = cl + RT;  // tiled fold: old m
-    float *xl = xm + RT;  // tiled fold: old l
-    if (tid < RT) {
+    // CTA statistics of each valid row: max, warp weights, sum.
+    if (tid < Gt) {
         float M = kNegInf;
+#pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * RT + tid]);
         float Lsum = 0.f;
+#pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float mw = wm[w * RT + tid];
             const float wt = mw == kNegInf ? 0.f : dev::exp2_approx(mw - M);
@@ -568,80 +588,128 @@ __global__ void __launch_bounds__(kThreads)
         cl[tid] = Lsum;
     }
     __syncthreads();
-    for (int e = tid; e < RT * DPAD; e += kThreads) {
-        const int g = e / DPAD, d = e - g * DPAD;
-        float acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) acc += ww[w * RT + g] * wo[(w * RT + g) * OSTRIDE + d];
-        co[g * OSTRIDE + d] = acc;
-    }
 
-    // ---- cluster merge (rank order) and epilogue -----------------------------------
-    // Rows are dealt to the cluster's ranks round-robin; each rank combines its
-    // rows over all ranks' results and writes them.
+    // ---- the unit's result: rows dealt to the cluster's ranks round-robin ------
+    // Row g of this rank combines the ranks' CTA results in rank order (C == 1:
+    // straight from the warp partials).  For every row the combine yields
+    // (M, L, O[d]); the epilogue then writes the output, the split's partial, or
+    // folds into the tiled running state.
     cg::cluster_group cluster = cg::this_cluster();
-    if (C > 1) cluster.sync(); else __syncthreads();
-
-    for (int g = part; g < Gt; g += C) {
-        const int h = h0 + g;
-        const long long row = static_cast<long long>(s) * Hq + h;
-        // combined (M, L) of row g
-        float M = kNegInf, Lsum = 0.f;
-        for (int rk = 0; rk < C; ++rk) {
-            const float *pm = C > 1 ? cluster.map_shared_rank(cm, rk) : cm;
-            M = fmaxf(M, pm[g]);
-        }
-        for (int rk = 0; rk < C; ++rk) {
-            const float *pm = C > 1 ? cluster.map_shared_rank(cm, rk) : cm;
-            const float *pl = C > 1 ? cluster.map_shared_rank(cl, rk) : cl;
-            const float mr = pm[g];
-            if (mr != kNegInf) Lsum += dev::exp2_approx(mr - M) * pl[g];
-        }
-        if constexpr (MODE == kModeTiled) {
-            if (tid == 0) {
-                xm[g] = p.st_m[row];
-                xl[g] = p.st_l[row];
-            }
-            __syncthreads();
-        }
-        for (int d = tid; d < D; d += kThreads) {
+    float *co = reinterpret_cast<float *>(smem + plan.result);  // [RT][OSTRIDE]
+    if (C > 1) {
+        for (int e = tid; e < Gt * DPAD; e += kThreads) {
+            const int g = e / DPAD, d = e - g * DPAD;
             float acc = 0.f;
-            for (int rk = 0; rk < C; ++rk) {
-                const float *pm = C > 1 ? cluster.map_shared_rank(cm, rk) : cm;
-                const float *po = C > 1 ? cluster.map_shared_rank(co, rk) : co;
-                const float mr = pm[g];
-                if (mr != kNegInf) acc += dev::exp2_approx(mr - M) * po[g * OSTRIDE + d];
-            }
-            if constexpr (MODE == kModePaged) {
-                if (direct) {
-                    const float v = Lsum > 0.f ? __fdiv_rn(acc, Lsum) : 0.f;
-                    p.out[row * D + d] = __float2bfloat16_rn(v);
-                } else {
-                    p.ws_o[(row * p.num_splits + split) * D + d] = acc;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) acc += ww[w * RT + g] * wo[(w * RT + g) * OSTRIDE + d];
+            co[g * OSTRIDE + d] = acc;
+        }
+        cluster.sync();
+    }
+    const int nmine = Gt > part ? (Gt - part + C - 1) / C : 0;  // rows g = part + i*C
+    // per-row factors: fx[i] = {M, L, a, b}; fr[i][rk] = weight of rank rk
+    if (tid < nmine) {
+        const int g = part + tid * C;
+        float M = kNegInf, Lsum = 0.f;
+        if (C > 1) {
+            float mr[kMaxCluster], lr[kMaxCluster];
+#pragma unroll
+            for (int rk = 0; rk < kMaxCluster; ++rk) {
+                if (rk < C) {
+                    mr[rk] = cluster.map_shared_rank(cm, rk)[g];
+                    lr[rk] = cluster.map_shared_rank(cl, rk)[g];
                 }
+            }
+#pragma unroll
+            for (int rk = 0; rk < kMaxCluster; ++rk)
+                if (rk < C) M = fmaxf(M, mr[rk]);
+#pragma unroll
+            for (int rk = 0; rk < kMaxCluster; ++rk) {
+                if (rk < C) {
+                    const float wt = mr[rk] == kNegInf ? 0.f : dev::exp2_approx(mr[rk] - M);
+                    fr[tid * kMaxCluster + rk] = wt;
+                    Lsum += wt * lr[rk];
+                }
+            }
+        } else {
+            M = cm[g];
+            Lsum = cl[g];
+        }
+        const long long row = static_cast<long long>(s) * Hq + h0 + g;
+        float fa = 0.f, fb = 0.f;
+        if constexpr (MODE == kModePaged) {
+            if (!direct) {
+                p.ws_ml[(row * p.num_splits + split) * 2 + 0] = M;
+                p.ws_ml[(row * p.num_splits + split) * 2 + 1] = Lsum;
             } else {
-                const float m_old = xm[g];
-                const float m_new = fmaxf(m_old, M);
-                const float a = m_old == kNegInf ? 0.f : dev::exp2_approx(m_old - m_new);
-                const float b = M == kNegInf ? 0.f : dev::exp2_approx(M - m_new);
-                float *so = p.st_o + row * D + d;
-                *so = *so * a + acc * b;
+                fb = Lsum > 0.f ? 1.f : 0.f;
+            }
+        } else {
+            const float m_old = p.st_m[row];
+            const float m_new = fmaxf(m_old, M);
+            fa = m_old == kNegInf ? 0.f : dev::exp2_approx(m_old - m_new);
+            fb = M == kNegInf ? 0.f : dev::exp2_approx(M - m_new);
+            p.st_l[row] = p.st_l[row] * fa + Lsum * fb;
+            p.st_m[row] = m_new;
+        }
+        fx[tid * 4 + 0] = M;
+        fx[tid * 4 + 1] = Lsum;
+        fx[tid * 4 + 2] = fa;
+        fx[tid * 4 + 3] = fb;
+    }
+    __syncthreads();
+    // elements (row i of this rank, column pair d)
+    const int halfD = D / 2;
+    for (int e = tid; e < nmine * halfD; e += kThreads) {
+        const int i = e / halfD;
+        const int d = (e - i * halfD) * 2;
+        const int g = part + i * C;
+        float acc0 = 0.f, acc1 = 0.f;
+        if (C > 1) {
+            float v0[kMaxCluster], v1[kMaxCluster];
+#pragma unroll
+            for (int rk = 0; rk < kMaxCluster; ++rk) {
+                if (rk < C) {
+                    const float2 v = *reinterpret_cast<const float2 *>(
+                        cluster.map_shared_rank(co, rk) + g * OSTRIDE + d);
+                    v0[rk] = v.x;
+                    v1[rk] = v.y;
+                }
+            }
+#pragma unroll
+            for (int rk = 0; rk < kMaxCluster; ++rk) {
+                if (rk < C) {
+                    acc0 += fr[i * kMaxCluster + rk] * v0[rk];
+                    acc1 += fr[i * kMaxCluster + rk] * v1[rk];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float wt = ww[w * RT + g];
+                acc0 += wt * wo[(w * RT + g) * OSTRIDE + d];
+                acc1 += wt * wo[(w * RT + g) * OSTRIDE + d + 1];
             }
         }
-        if (tid == 0) {
-            if constexpr (MODE == kModePaged) {
-                if (!direct) {
-                    p.ws_ml[(row * p.num_splits + split) * 2 + 0] = M;
-                    p.ws_ml[(row * p.num_splits + split) * 2 + 1] = Lsum;
-                }
+        const long long row = static_cast<long long>(s) * Hq + h0 + g;
+        if constexpr (MODE == kModePaged) {
+            if (direct) {
+                const float Lsum = fx[i * 4 + 1];
+                const bool pos = fx[i * 4 + 3] > 0.f;
+                const __nv_bfloat162 v = __floats2bfloat162_rn(pos ? __fdiv_rn(acc0, Lsum) : 0.f,
+                                                               pos ? __fdiv_rn(acc1, Lsum) : 0.f);
+                *reinterpret_cast<__nv_bfloat162 *>(p.out + row * D + d) = v;
             } else {
-                const float m_old = xm[g];
-                const float m_new = fmaxf(m_old, M);
-                const float a = m_old == kNegInf ? 0.f : dev::exp2_approx(m_old - m_new);
-                const float b = M == kNegInf ? 0.f : dev::exp2_approx(M - m_new);
-                p.st_l[row] = xl[g] * a + Lsum * b;
-                p.st_m[row] = m_new;
+                *reinterpret_cast<float2 *>(p.ws_o + (row * p.num_splits + split) * D + d) =
+                    make_float2(acc0, acc1);
             }
+        } else {
+            const float fa = fx[i * 4 + 2], fb = fx[i * 4 + 3];
+            float2 *so = reinterpret_cast<float2 *>(p.st_o + row * D + d);
+            float2 cur = *so;
+            cur.x = cur.x * fa + acc0 * fb;
+            cur.y = cur.y * fa + acc1 * fb;
+            *so = cur;
         }
     }
     if (C > 1) cluster.sync();  // peers keep their shared memory until every rank has read it

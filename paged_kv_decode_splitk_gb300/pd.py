@@ -96,7 +96,7 @@ _SIGS = {
     "pd_tiled_finalize": (_I, [_VP, _VP, _I, _VP]),
     "pd_device_status": (_I, [_VP]),
     "pd_debug_fail_next_allocs": (None, [_I]),
-    "pd_debug_set_tuning": (None, [_I, _I, _I, _I]),
+    "pd_debug_set_tuning": (None, [_I, _I, _I]),
 }
 
 
@@ -359,6 +359,5 @@ def pd_debug_fail_next_allocs(count: int) -> None:
     lib().pd_debug_fail_next_allocs(count)
 
 
-def pd_debug_set_tuning(stages_per_warp: int = 0, cluster: int = 0, prefetch: int = -1,
-                        longest_first: int = -1) -> None:
-    lib().pd_debug_set_tuning(stages_per_warp, cluster, prefetch, longest_first)
+def pd_debug_set_tuning(stages_per_warp: int = 0, cluster: int = 0, longest_first: int = -1) -> None:
+    lib().pd_debug_set_tuning(stages_per_warp, cluster, longest_first)
