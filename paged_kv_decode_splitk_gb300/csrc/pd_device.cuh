@@ -59,12 +59,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
-// Order this thread's generic-proxy shared-memory accesses before later
-// async-proxy (TMA) accesses to the same memory.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- TMA ------------------------------------------------------------------
 // 4-D tiled tensor load global -> shared, completion counted in bytes on `bar`.
 // The L2 hint marks the lines evict-first: every K/V byte is read once.

@@ -388,9 +388,10 @@ __global__ void __launch_bounds__(kThreads)
                 dev::mma_bf16_16816(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
             }
         }
-        // the K half is read: refill it with tile r + S
+        // The K half is read (every lane's ldmatrix result has been consumed by
+        // an mma): refill it with tile r + S.  A read-then-overwrite by the TMA
+        // needs no proxy fence once the read values are in registers.
         if (rn < nloc) {
-            dev::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) issue(&tmk, 0, rn, k, id_next);
         }
@@ -505,7 +506,6 @@ __global__ void __launch_bounds__(kThreads)
         }
         // the V half is read: refill it with tile r + S
         if (rn < nloc) {
-            dev::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) issue(&tmv, 1, rn, k, id_next);
         }
