@@ -198,6 +198,40 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
                    float inv_sqrt_d, int num_splits, void *workspace, size_t workspace_bytes,
                    int gqa_pack, void *stream);
 
+/* Size of the library-owned split-K workspace behind pd_decode_attn_noalloc. */
+#define PD_NOALLOC_WORKSPACE_BYTES 16777216u /* 16 MiB */
+
+/* pd_decode_attn_noalloc: pd_decode_attn for callers that cannot allocate
+ * device memory.  The pages this library follows describe no counterpart; it
+ * exists for code that must not call cudaMalloc on the decode path: an
+ * application whose device memory is all reserved up front by its own pool
+ * allocator, or a plug-in that may not grow the host program's footprint,
+ * and any caller for whom the implicit device synchronisation and locking of
+ * cudaMalloc / cudaFree are not acceptable there.
+ *
+ * Arguments, shapes, results and error codes are those of pd_decode_attn
+ * without workspace / workspace_bytes: the split-K workspace is a fixed
+ * PD_NOALLOC_WORKSPACE_BYTES array that libpd holds in every GPU's memory
+ * from the moment the library's kernels are loaded on it until the process
+ * exits.  A launch whose workspace (pd_workspace_bytes(num_seqs, num_q_heads,
+ * head_dim, num_splits), 0 when num_splits == 1) would exceed that size is
+ * rejected with PD_ERR_WORKSPACE and launches nothing.  Nothing is allocated,
+ * by this call or by anything it calls.
+ *
+ * The first call on a device looks up that device's address of the array
+ * (cudaGetSymbolAddress, with the device current); make that first call
+ * before any stream capture.  All calls on a device share the one array and
+ * it keeps the previous call's contents; no part of it needs to start at zero
+ * (every value a call reads is written earlier in the same call), but two
+ * calls whose kernels overlap on the GPU, on different streams or from
+ * different threads, race on it and may produce garbage: serialise them. */
+int pd_decode_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_table, int max_blocks_per_seq,
+                           const int32_t *context_lens, void *out, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, float inv_sqrt_d, int num_splits, int gqa_pack,
+                           void *stream);
+
 /* ---- tiled decode (tiled_attention.rs page) ------------------------------ */
 
 /* TiledAttentionDims: the state is sized for max_seqs sequences. */

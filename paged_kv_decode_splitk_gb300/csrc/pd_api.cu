@@ -288,6 +288,10 @@ int check_shape(int num_q_heads, int num_kv_heads, int head_dim, int block_size)
 
 }  // namespace
 
+namespace pd {
+int report_error(int code, const char *message) { return fail(code, "%s", message); }
+}  // namespace pd
+
 struct pd_tiled {
     pd_tiled_dims dims;
     float *m;

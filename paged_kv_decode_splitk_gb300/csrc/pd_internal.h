@@ -82,6 +82,9 @@ struct MergeParams {
     int max_tokens;  // max_blocks_per_seq * block_size (context lengths are clamped to it)
 };
 
+// Record an error message for pd_last_error() and return `code`.
+int report_error(int code, const char *message);
+
 // Dynamic shared memory a unit CTA needs.
 int unit_smem_bytes(int dpad, int rows, int stages);
 

@@ -83,6 +83,8 @@ _SIGS = {
     "pd_split_chunk_tokens": (_I, [_I, _I, _I]),
     "pd_decode_attn": (_I, [_VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I,
                             ctypes.c_float, _I, _VP, _SZ, _I, _VP]),
+    "pd_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I,
+                                    ctypes.c_float, _I, _I, _VP]),
     "pd_tiled_validate": (_I, [_VP]),
     "pd_tiled_state_bytes": (_I, [_VP, _VP, _VP, _VP, _VP]),
     "pd_tiled_create": (_I, [_VP, _VP]),
@@ -242,6 +244,22 @@ def pd_decode_attn(q, k_cache, v_cache, block_table, context_lens, out, inv_sqrt
                               D, bs, nb if num_blocks is None else num_blocks, float(inv_sqrt_d),
                               int(num_splits), _ptr(workspace), ws_bytes, int(bool(gqa_pack)),
                               _stream(stream))
+    return _check(rc)
+
+
+def pd_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, out, inv_sqrt_d: float,
+                           num_splits: int, gqa_pack: bool = False, stream=None,
+                           num_blocks: int | None = None) -> int:
+    """pd_decode_attn with the split-K workspace held by the library (see pd.h): for
+    callers that cannot allocate device memory.  Same tensors and shapes, no workspace."""
+    S, Hq, D = q.shape
+    nb, bs, Hkv, D2 = k_cache.shape
+    assert D2 == D, "head_dim mismatch"
+    rc = lib().pd_decode_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                      int(block_table.shape[1]), _ptr(context_lens), _ptr(out), S, Hq,
+                                      Hkv, D, bs, nb if num_blocks is None else num_blocks,
+                                      float(inv_sqrt_d), int(num_splits), int(bool(gqa_pack)),
+                                      _stream(stream))
     return _check(rc)
 
 
