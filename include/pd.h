@@ -320,12 +320,11 @@ int pd_device_status(int *flags);
 void pd_debug_fail_next_allocs(int count);
 
 /* Tuning hook for launch-shape experiments, applied to the following launches
- * in this process: pipeline stages per warp (1..8; 0 = built-in), CTAs per
- * unit cluster (1..8; 0 = built-in) and longest-first service order of small
- * batches (0/1; -1 = built-in).  Stages and order change only timing.  A
- * cluster size other than the built-in one changes the summation order and so
- * the output bits (still within tolerance): never change it between launches
- * whose outputs must be bit-identical. */
+ * in this process: pipeline stages per warp (1..8; 0 = built-in), where the
+ * parts of a unit run (0 = chosen from occupancy, 1 = one CTA per unit, > 1 =
+ * one CTA per part in a thread-block cluster) and longest-first service order
+ * of small batches (0/1; -1 = built-in).  None of them changes the output
+ * bits: the parts and their fold order depend only on each sequence. */
 void pd_debug_set_tuning(int stages_per_warp, int cluster, int longest_first);
 
 #if defined(__GNUC__)

@@ -239,27 +239,26 @@ int default_lpt(int num_seqs) {
     return on && num_seqs <= pd::kLptMaxSeqs ? 1 : 0;
 }
 
-// CTAs per packed unit: the packed pass has only num_kv_heads * num_seqs
-// units, so each is spread over a cluster that merges through distributed
-// shared memory.  A build constant (it fixes the summation order).
-constexpr int kPackCluster = 6;
-
-// CTAs per tiled unit (same role for step_tile's (sequence, KV head) units).
-constexpr int kTiledCluster = 2;
+// A unit's range (one split of a sequence, or one tile of it) is cut into up
+// to max_parts parts of about kPartTiles 16-token tiles, by its own length; the
+// parts fold in order.  Build constants: they fix the summation order.
+constexpr int kPartTiles = 32;
+int max_parts_for(int dpad, bool tiled) { return tiled ? 2 : (dpad >= 256 ? 6 : 4); }
 
 int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
 
 template <int MODE>
 cudaError_t dispatch_unit(int dpad, int gn, bool hl, bool packed, const CUtensorMap &tk,
-                          const CUtensorMap &tv, const pd::UnitParams &p, int grid_x, int smem,
+                          const CUtensorMap &tv, const pd::UnitParams &p, long long units, int smem,
                           cudaStream_t st) {
     using namespace pd;
-    if (packed) return launch_unit<256, 1, false, kModePaged, true>(tk, tv, p, grid_x, smem, st);
-#define PD_DISPATCH_D(DP)                                                                   \
-    if (dpad == DP) {                                                                       \
-        if (gn == 2) return launch_unit<DP, 2, false, MODE, false>(tk, tv, p, grid_x, smem, st); \
-        if (hl) return launch_unit<DP, 1, true, MODE, false>(tk, tv, p, grid_x, smem, st);       \
-        return launch_unit<DP, 1, false, MODE, false>(tk, tv, p, grid_x, smem, st);              \
+    const int layout = g_debug_cluster == 1 ? 1 : (g_debug_cluster > 1 ? 2 : 0);
+    if (packed) return launch_unit<256, 1, false, kModePaged, true>(tk, tv, p, units, smem, st, layout);
+#define PD_DISPATCH_D(DP)                                                                          \
+    if (dpad == DP) {                                                                              \
+        if (gn == 2) return launch_unit<DP, 2, false, MODE, false>(tk, tv, p, units, smem, st, layout); \
+        if (hl) return launch_unit<DP, 1, true, MODE, false>(tk, tv, p, units, smem, st, layout);       \
+        return launch_unit<DP, 1, false, MODE, false>(tk, tv, p, units, smem, st, layout);              \
     }
     PD_DISPATCH_D(64)
     PD_DISPATCH_D(128)
@@ -508,11 +507,10 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     const int gn = packed ? 1 : (G <= 8 ? 1 : 2);
     const int rows = 8 * gn;
     const int qtiles = (G + rows - 1) / rows;
-    int cluster = packed ? kPackCluster : 1;
-    if (g_debug_cluster > 0) cluster = g_debug_cluster;
     const int stages = default_stages(dpad);
-    const long long grid = static_cast<long long>(num_seqs) * num_kv_heads * qtiles * num_splits * cluster;
-    if (grid > 0x7fffffffLL) return fail(PD_ERR_INVALID, "launch too large (%lld CTAs)", grid);
+    const long long units = static_cast<long long>(num_seqs) * num_kv_heads * qtiles * num_splits;
+    if (units * max_parts_for(dpad, false) > 0x7fffffffLL)
+        return fail(PD_ERR_INVALID, "launch too large (%lld units)", units);
 
     int err = PD_OK;
     unsigned int *status = status_ptr(&err);
@@ -549,7 +547,9 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     p.head_dim = head_dim;
     p.block_size = block_size;
     p.qtiles = qtiles;
-    p.cluster = cluster;
+    p.cluster = 1;
+    p.max_parts = max_parts_for(dpad, false);
+    p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = default_lpt(num_seqs);
     p.tok_dim = tok_dim;
@@ -561,8 +561,8 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     if (smem > max_smem_optin())
         return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
                     smem, max_smem_optin());
-    cudaError_t e = dispatch_unit<pd::kModePaged>(dpad, gn, !packed && G <= 4, packed, tk, tv, p,
-                                                  static_cast<int>(grid), smem, st);
+    cudaError_t e = dispatch_unit<pd::kModePaged>(dpad, gn, !packed && G <= 4, packed, tk, tv, p, units,
+                                                  smem, st);
     if (e != cudaSuccess) return cuda_fail(e, "unit kernel launch");
     if (num_splits > 1) {
         pd::MergeParams mp = {};
@@ -731,11 +731,9 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     const int gn = G <= 8 ? 1 : 2;
     const int rows = 8 * gn;
     const int qtiles = (G + rows - 1) / rows;
-    int cluster = kTiledCluster;
-    if (g_debug_cluster > 0) cluster = g_debug_cluster;
     const int stages = default_stages(dpad);
-    const long long grid = static_cast<long long>(num_seqs) * d.num_kv_heads * qtiles * cluster;
-    if (grid > 0x7fffffffLL) return fail(PD_ERR_INVALID, "launch too large");
+    const long long units = static_cast<long long>(num_seqs) * d.num_kv_heads * qtiles;
+    if (units * max_parts_for(dpad, true) > 0x7fffffffLL) return fail(PD_ERR_INVALID, "launch too large");
 
     int err = PD_OK;
     unsigned int *status = status_ptr(&err);
@@ -766,7 +764,9 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     p.head_dim = d.head_dim;
     p.block_size = d.block_size;
     p.qtiles = qtiles;
-    p.cluster = cluster;
+    p.cluster = 1;
+    p.max_parts = max_parts_for(dpad, true);
+    p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = 0;
     p.tok_dim = tok_dim;
@@ -778,8 +778,7 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     if (smem > max_smem_optin())
         return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
                     smem, max_smem_optin());
-    cudaError_t e = dispatch_unit<pd::kModeTiled>(dpad, gn, G <= 4, false, tk, tv, p,
-                                                  static_cast<int>(grid), smem,
+    cudaError_t e = dispatch_unit<pd::kModeTiled>(dpad, gn, G <= 4, false, tk, tv, p, units, smem,
                                                   static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tiled step launch");
     return ok();
@@ -822,7 +821,7 @@ void pd_debug_fail_next_allocs(int count) { g_fail_allocs.store(count < 0 ? 0 : 
 
 void pd_debug_set_tuning(int stages_per_warp, int cluster, int longest_first) {
     g_debug_stages = stages_per_warp > 0 && stages_per_warp <= pd::kMaxStagesPerWarp ? stages_per_warp : 0;
-    g_debug_cluster = cluster > 0 && cluster <= pd::kMaxCluster ? cluster : 0;
+    g_debug_cluster = cluster == 1 ? 1 : (cluster > 1 ? 2 : 0);
     g_debug_lpt = longest_first == 0 || longest_first == 1 ? longest_first : -1;
 }
 

@@ -17,7 +17,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTileTokens = 16;   // tokens per mma tile (the K/V stage)
 constexpr int kBoxCols = 64;      // BF16 columns per TMA box (128 bytes, 128B swizzle)
 constexpr int kMaxStagesPerWarp = 8;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxParts = 8;   // parts of a unit (and CTAs of a unit cluster) at most
 constexpr int kLptMaxSeqs = 64;
 
 // Tokens per split (module description of attn_splitk: the split size is
@@ -65,7 +65,9 @@ struct UnitParams {
     // shape
     int num_seqs, num_q_heads, num_kv_heads, group, head_dim, block_size;
     int qtiles;       // CTAs per (s, kvh): ceil(group / rows per CTA)
-    int cluster;      // CTAs per unit (thread-block cluster size)
+    int cluster;      // CTAs per unit: 1 (parts in sequence) or max_parts (one part per CTA)
+    int max_parts;    // parts a unit's range is cut into at most
+    int part_tiles;   // tiles per part the cut aims for
     int stages;       // pipeline stages per warp
     int lpt;          // paged mode: serve sequences longest first (needs num_seqs <= kLptMaxSeqs)
     int tok_dim;      // tensor-map dimension of the token coordinate (1 or 2)
@@ -89,9 +91,10 @@ int report_error(int code, const char *message);
 int unit_smem_bytes(int dpad, int rows, int stages);
 
 // Kernel launchers (defined in the per-head-dim translation units).
+// layout: 0 = choose from occupancy, 1 = one CTA per unit, 2 = one CTA per part.
 template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
 cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p,
-                        int grid_x, int smem_bytes, cudaStream_t stream);
+                        long long units, int smem_bytes, cudaStream_t stream, int layout);
 
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream, bool programmatic);
 cudaError_t launch_tiled_begin(float *m, float *l, float *o, int rows, int head_dim,

@@ -57,6 +57,20 @@ constexpr unsigned int kDevBadContextLen = 2;
 constexpr unsigned int kDevBadTileCount = 4;
 constexpr unsigned int kDevWaitTimeout = 8;
 
+// Left fold of two (m, l, o) states in base 2: the running state R and the
+// next part P give M = max(mR, mP), a = 2^(mR - M), b = 2^(mP - M) (0 for an
+// empty side), l = lR*a + lP*b, o = oR*a + oP*b.  Rounding is pinned (no
+// contraction) so that every place that folds computes the same bits.
+__device__ __forceinline__ void fold_factors(float mr, float mp, float &mn, float &a, float &b) {
+    const float kNegInf = -__int_as_float(0x7f800000);
+    mn = fmaxf(mr, mp);
+    a = mr == kNegInf ? 0.f : dev::exp2_approx(mr - mn);
+    b = mp == kNegInf ? 0.f : dev::exp2_approx(mp - mn);
+}
+__device__ __forceinline__ float fold_value(float r, float a, float pv, float b) {
+    return __fadd_rn(__fmul_rn(r, a), __fmul_rn(pv, b));
+}
+
 // Shared-memory plan of a unit CTA (host and device agree on it).  Offsets are
 // from the 1024-byte-aligned base.  The warp-merge area and the CTA result
 // reuse the stage ring once every tile has been consumed.
@@ -65,14 +79,14 @@ struct UnitSmem {
     int merge;   // per-warp o [kWarps][rows][dpad+4]: overlaps the ring
     int result;  // CTA result o [rows][dpad+4], read by the cluster peers: overlaps the ring
     int qs;      // the CTA's query rows, BF16, padded rows
-    int stats;   // per-warp m, l, weights; CTA m, l; row factors of the final combine
+    int stats;   // per-warp m, l, weights; part m, l; row factors; fold factors; running m, l
     int bars;    // two mbarriers (K, V) per stage
     int lpt;     // longest-first order: context lengths + the pick
     int total;   // bytes to request, including the alignment slack
 };
 
 __host__ __device__ constexpr int unit_stat_floats(int rows) {
-    return rows * (3 * kWarps + 2 + 4 + kMaxCluster);
+    return rows * (3 * kWarps + 2 + 4 + 2 * kMaxParts + 2);
 }
 
 __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stages_per_warp) {
@@ -241,13 +255,13 @@ __global__ void __launch_bounds__(kThreads)
         ids_base = p.tile_blocks + static_cast<long long>(s) * p.tile_capacity;
     }
 
-    // 16-token tiles of the range, split across the cluster's CTAs.
+    // 16-token tiles of the range, cut into V parts of about p.part_tiles tiles
+    // (at most p.max_parts).  V depends only on the range's own length; the
+    // launch decides only where the parts run: all in this CTA one after
+    // another (cluster == 1), or one per CTA of a cluster (cluster == max_parts).
     const int tile0 = tok0 / kTileTokens;
     const int ntiles = (tok1 + kTileTokens - 1) / kTileTokens - tile0;
-    const int per = (ntiles + C - 1) / C;
-    const int my0 = tile0 + min(part * per, ntiles);
-    const int my1 = tile0 + min((part + 1) * per, ntiles);
-    const int nloc = my1 - my0 > warp ? (my1 - my0 - warp + kWarps - 1) / kWarps : 0;
+    const int V = max(1, min(p.max_parts, (ntiles + p.part_tiles - 1) / p.part_tiles));
 
     // ---- q to shared memory (the barriers were initialised at the start) ----------
 #pragma unroll
@@ -257,53 +271,23 @@ __global__ void __launch_bounds__(kThreads)
         const int d = (e - g * (DPAD / 2)) * 2;
         *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) = qv[i];
     }
+    // Running result of the parts folded so far (cluster == 1), starting empty:
+    // m and l per row in shared memory, o in registers (element e = tid + i *
+    // kThreads of the [RT][DPAD] rows, the same elements for every part).
+    constexpr int RACC = RT * DPAD / kThreads;
+    float racc[RACC];
+#pragma unroll
+    for (int i = 0; i < RACC; ++i) racc[i] = 0.f;
+    float *rM = stats + unit_stat_floats(RT) - 2 * RT;  // [RT]
+    float *rL = rM + RT;                                 // [RT]
+    if (tid < RT) {
+        rM[tid] = kNegInf;
+        rL[tid] = 0.f;
+    }
     __syncthreads();
 
     const uint64_t policy = dev::l2_evict_first_policy();
     const int tiles_per_block = bs / kTileTokens;
-
-    // Block id of this warp's local tile r (lane-parallel window loads).
-    auto load_id = [&](int r) -> int {
-        if (r >= nloc) return -1;
-        const int gt = my0 + warp + kWarps * r;
-        const int j = gt / tiles_per_block;
-        int id = __ldg(ids_base + j);
-        // TMA reads zeros outside the tensor map's block extent (num_blocks).
-        if (id < 0 || id >= p.num_blocks) dev::flag_status(p.status, kDevBadBlockId);
-        return id;
-    };
-    // TMA of the K (half 0) or V (half 1) tile of local tile r into stage k.
-    auto issue = [&](const CUtensorMap *map, int half, int r, int k, int id) {
-        const int gt = my0 + warp + kWarps * r;
-        const int sub = (gt % tiles_per_block) * kTileTokens;
-        const uint32_t bar = dev::smem_addr(&bars[(warp * S + k) * 2 + half]);
-        const uint32_t dst = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES + half * TILE_BYTES);
-        const int c1 = p.tok_dim == 1 ? sub : kvh;
-        const int c2 = p.tok_dim == 1 ? kvh : sub;
-        dev::mbar_arrive_expect_tx(bar, TILE_BYTES);
-#pragma unroll
-        for (int b = 0; b < NBOX; ++b)
-            dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * kBoxCols, c1, c2, id, policy);
-    };
-
-    // Block ids of local tiles [32*win, 32*win + 64): lane l of id_cur holds
-    // tile 32*win + l, lane l of id_nxt tile 32*win + 32 + l.
-    int win = 0;
-    int id_cur = load_id(lane);
-    int id_nxt = load_id(32 + lane);
-    auto id_at = [&](int r) -> int {
-        const int a = __shfl_sync(0xffffffffu, id_cur, r & 31);
-        const int b = __shfl_sync(0xffffffffu, id_nxt, r & 31);
-        return (r >> 5) == win ? a : b;
-    };
-    const int npro = nloc < S ? nloc : S;
-    for (int r = 0; r < npro; ++r) {
-        const int id = __shfl_sync(0xffffffffu, id_cur, r);
-        if (lane == 0) {
-            issue(&tmk, 0, r, r, id);
-            issue(&tmv, 1, r, r, id);
-        }
-    }
 
     // B operand of S^T = K q^T (q^T: d x g), one x2 ldmatrix per k-step and
     // n-tile: lanes 0-7 address rows g of columns k0..k0+7, lanes 8-15 k0+8..15.
@@ -322,281 +306,326 @@ __global__ void __launch_bounds__(kThreads)
         lmv_off[c2] = tv * 128 + ((((2 * c2) + (lm_j & 1)) ^ (lane & 7)) << 4);
     }
 
-    // ---- online-softmax state ---------------------------------------------------
-    // Accumulator layouts (m16n8 fragments): S^T[t][g] with t = lane/4 (+8),
-    // g = nt*8 + (lane%4)*2 (+1); O^T[d][g] with d = mt*16 + lane/4 (+8) and the
-    // same g.  Each thread keeps (m, l) of its two columns g.  With HL (groups of
-    // at most 4) columns 4..7 of the single n-tile carry the BF16 residual of P
-    // for columns 0..3, so one mma per m-tile serves both halves of P.
     const int tq = lane >> 2;         // token row of the S^T fragment
     const int gq = (lane & 3) * 2;    // first column (group row) of this thread
-    float o[KS][GN][4];
-#pragma unroll
-    for (int a_ = 0; a_ < KS; ++a_)
-#pragma unroll
-        for (int b_ = 0; b_ < GN; ++b_)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) o[a_][b_][c] = 0.f;
-    float m_run[GN][2], l_run[GN][2];
-#pragma unroll
-    for (int nt = 0; nt < GN; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            m_run[nt][c] = kNegInf;
-            l_run[nt][c] = 0.f;
-        }
-    int fail_r = -1;
-
-    for (int r = 0; r < nloc; ++r) {
-        const int k = r % S;
-        const uint32_t par = (r / S) & 1;
-        const int rn = r + S;
-        int id_next = -1;
-        if (rn < nloc) {
-            if ((rn >> 5) != win) {
-                id_cur = id_nxt;
-                win = rn >> 5;
-                id_nxt = load_id((win + 1) * 32 + lane);
-            }
-            id_next = id_at(rn);
-        }
-        if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 0]), par)) {
-            fail_r = r;
-            break;
-        }
-        const int gt = my0 + warp + kWarps * r;
-        const int nvalid = min(kTileTokens, tok1 - gt * kTileTokens);
-        const uint32_t kbase = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES);
-        const uint32_t vbase = kbase + TILE_BYTES;
-
-        // S^T = K . q^T, two accumulator chains (even / odd k-steps)
-        float sc[GN][2][4];
-#pragma unroll
-        for (int nt = 0; nt < GN; ++nt)
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) sc[nt][h2][c] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            dev::ldsm_x4(kbase + (ks >> 2) * (kTileTokens * 128) + lmk_off[ks & 3], a0, a1, a2, a3);
-#pragma unroll
-            for (int nt = 0; nt < GN; ++nt) {
-                uint32_t b0, b1;
-                dev::ldsm_x2(q_lm + nt * 8 * QST + ks * 32, b0, b1);
-                dev::mma_bf16_16816(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
-            }
-        }
-        // The K half is read (every lane's ldmatrix result has been consumed by
-        // an mma): refill it with tile r + S.  A read-then-overwrite by the TMA
-        // needs no proxy fence once the read values are in registers.
-        if (rn < nloc) {
-            __syncwarp();
-            if (lane == 0) issue(&tmk, 0, rn, k, id_next);
-        }
-
-        // column softmax over the tile's tokens, base 2, tokens past the range masked
-        float alpha[GN][2];
-        float pv[GN][4];
-#pragma unroll
-        for (int nt = 0; nt < GN; ++nt) {
-            float x[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int t = tq + (c >> 1) * 8;
-                const float v = (sc[nt][0][c] + sc[nt][1][c]) * p.scale_log2;
-                x[c] = t < nvalid ? v : kNegInf;
-            }
-            float cmx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                cmx[0] = fmaxf(cmx[0], __shfl_xor_sync(0xffffffffu, cmx[0], off));
-                cmx[1] = fmaxf(cmx[1], __shfl_xor_sync(0xffffffffu, cmx[1], off));
-            }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const float m_new = fmaxf(m_run[nt][c], cmx[c]);
-                alpha[nt][c] = dev::exp2_approx(m_run[nt][c] - m_new);
-                const float e0 = dev::exp2_approx(x[c] - m_new);
-                const float e1 = dev::exp2_approx(x[c + 2] - m_new);
-                pv[nt][c] = e0;
-                pv[nt][c + 2] = e1;
-                l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + (e0 + e1);
-                m_run[nt][c] = m_new;
-            }
-        }
-
-        // P^T as the B operand of O^T += V^T P^T: pack to BF16 (high part and
-        // residual) and transpose each 8x8 block in registers.
-        uint32_t bh[GN][2], bl[GN][2];
-#pragma unroll
-        for (int nt = 0; nt < GN; ++nt)
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const float e0 = pv[nt][2 * h2], e1 = pv[nt][2 * h2 + 1];
-                const uint32_t hi = dev::pack_bf16x2(e0, e1);
-                const uint32_t lo = dev::pack_bf16x2(e0 - dev::bf16_lo_f32(hi), e1 - dev::bf16_hi_f32(hi));
-                bh[nt][h2] = dev::movmatrix_trans(hi);
-                bl[nt][h2] = dev::movmatrix_trans(lo);
-            }
-        if constexpr (HL) {
-            // lanes 16..31 hold rows g = 4..7 of the transposed blocks: give them
-            // the residual of rows 0..3 instead
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const uint32_t lo_src = __shfl_sync(0xffffffffu, bl[0][h2], lane & 15);
-                bh[0][h2] = lane < 16 ? bh[0][h2] : lo_src;
-            }
-        }
-
-        // rescale O^T columns whose max moved (HL: columns 4..7 follow 0..3)
-        bool any = false;
-#pragma unroll
-        for (int nt = 0; nt < GN; ++nt) any |= (alpha[nt][0] != 1.f) | (alpha[nt][1] != 1.f);
-        if (__any_sync(0xffffffffu, any)) {
-#pragma unroll
-            for (int nt = 0; nt < GN; ++nt) {
-                float a0 = alpha[nt][0], a1 = alpha[nt][1];
-                if constexpr (HL) {
-                    const float p0 = __shfl_xor_sync(0xffffffffu, a0, 2);
-                    const float p1 = __shfl_xor_sync(0xffffffffu, a1, 2);
-                    if (lane & 2) {
-                        a0 = p0;
-                        a1 = p1;
-                    }
-                }
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    o[mt][nt][0] *= a0;
-                    o[mt][nt][1] *= a1;
-                    o[mt][nt][2] *= a0;
-                    o[mt][nt][3] *= a1;
-                }
-            }
-        }
-
-        if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 1]), par)) {
-            fail_r = r;
-            break;
-        }
-        // O^T += V^T . P^T  (V rows past the range may hold anything: mask them)
-        auto pv_tile = [&](uint32_t mask01, uint32_t mask89) {
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                uint32_t a0, a1, a2, a3;
-                dev::ldsm_x4_trans(vbase + (mt >> 2) * (kTileTokens * 128) + lmv_off[mt & 3], a0, a1, a2, a3);
-                a0 &= mask01;
-                a1 &= mask01;
-                a2 &= mask89;
-                a3 &= mask89;
-#pragma unroll
-                for (int nt = 0; nt < GN; ++nt) {
-                    dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                    if constexpr (!HL) dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
-                }
-            }
-        };
-        if (nvalid == kTileTokens) {
-            pv_tile(0xffffffffu, 0xffffffffu);
-        } else {
-            const int tv0 = (lane & 3) * 2;
-            pv_tile((tv0 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 1 < nvalid ? 0xffff0000u : 0u),
-                    (tv0 + 8 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 9 < nvalid ? 0xffff0000u : 0u));
-        }
-        // the V half is read: refill it with tile r + S
-        if (rn < nloc) {
-            __syncwarp();
-            if (lane == 0) issue(&tmv, 1, rn, k, id_next);
-        }
-    }
-    if (fail_r >= 0) {
-        // A bounded wait ran out.  Record it and drain (bounded) whatever this
-        // warp may still have in flight before the ring is reused.
-        if (lane == 0) dev::flag_status(p.status, kDevWaitTimeout);
-        const int last = fail_r + S + 1 < nloc ? fail_r + S + 1 : nloc;
-        for (int r = fail_r; r < last; ++r)
-            for (int h = 0; h < 2; ++h)
-                dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + r % S) * 2 + h]), (r / S) & 1,
-                                       100000000ull);
-    }
-
-    // ---- warp merge (fixed warp order) -------------------------------------------
-    // column sums over the tokens of all lanes of a column
-#pragma unroll
-    for (int nt = 0; nt < GN; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1)
-                l_run[nt][c] += __shfl_xor_sync(0xffffffffu, l_run[nt][c], off);
-    if constexpr (HL) {
-        // columns 0..3 = high part + residual held in columns 4..7
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) o[mt][0][c] += __shfl_xor_sync(0xffffffffu, o[mt][0][c], 2);
-    }
-    __syncthreads();  // every warp is done with the ring; reuse it for the merge
     float *wo = reinterpret_cast<float *>(smem + plan.merge);  // [kWarps][RT][OSTRIDE]
     float *wm = stats;                                         // [kWarps][RT]
     float *wl = wm + kWarps * RT;                              // [kWarps][RT]
     float *ww = wl + kWarps * RT;                              // [kWarps][RT] weights
-    float *cm = ww + kWarps * RT;                              // [RT] CTA max
-    float *cl = cm + RT;                                       // [RT] CTA sum
+    float *cm = ww + kWarps * RT;                              // [RT] part max
+    float *cl = cm + RT;                                       // [RT] part sum
     float *fx = cl + RT;                                       // [RT][4] row factors of the final combine
-    float *fr = fx + 4 * RT;                                   // [RT][kMaxCluster] rank weights
+    float *fr = fx + 4 * RT;                                   // [RT][2*kMaxParts] fold factors
+    float *co = reinterpret_cast<float *>(smem + plan.result);  // [RT][OSTRIDE] part result
     constexpr int GCOLS = HL ? 4 : 8;  // meaningful columns per n-tile
-    if (tq == 0) {
+
+    int rr = 0;  // tiles this warp has taken through its ring so far (stage phases)
+    const int jfirst = C == 1 ? 0 : part;
+    const int jstep = C == 1 ? 1 : C;
+    for (int j = jfirst; j < V; j += jstep) {
+        const int my0 = tile0 + (j * ntiles) / V;
+        const int my1 = tile0 + ((j + 1) * ntiles) / V;
+        const int nloc = my1 - my0 > warp ? (my1 - my0 - warp + kWarps - 1) / kWarps : 0;
+
+        // Block id of this warp's local tile r of the part (lane-parallel window loads).
+        auto load_id = [&](int r) -> int {
+            if (r >= nloc) return -1;
+            const int gt = my0 + warp + kWarps * r;
+            int id = __ldg(ids_base + gt / tiles_per_block);
+            // TMA reads zeros outside the tensor map's block extent (num_blocks).
+            if (id < 0 || id >= p.num_blocks) dev::flag_status(p.status, kDevBadBlockId);
+            return id;
+        };
+        // TMA of the K (half 0) or V (half 1) tile of local tile r into stage k.
+        auto issue = [&](const CUtensorMap *map, int half, int r, int k, int id) {
+            const int gt = my0 + warp + kWarps * r;
+            const int sub = (gt % tiles_per_block) * kTileTokens;
+            const uint32_t bar = dev::smem_addr(&bars[(warp * S + k) * 2 + half]);
+            const uint32_t dst = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES + half * TILE_BYTES);
+            const int c1 = p.tok_dim == 1 ? sub : kvh;
+            const int c2 = p.tok_dim == 1 ? kvh : sub;
+            dev::mbar_arrive_expect_tx(bar, TILE_BYTES);
+#pragma unroll
+            for (int b = 0; b < NBOX; ++b)
+                dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * kBoxCols, c1, c2, id, policy);
+        };
+
+        // Block ids of local tiles [32*win, 32*win + 64): lane l of id_cur holds
+        // tile 32*win + l, lane l of id_nxt tile 32*win + 32 + l.
+        int win = 0;
+        int id_cur = load_id(lane);
+        int id_nxt = load_id(32 + lane);
+        auto id_at = [&](int r) -> int {
+            const int a = __shfl_sync(0xffffffffu, id_cur, r & 31);
+            const int b = __shfl_sync(0xffffffffu, id_nxt, r & 31);
+            return (r >> 5) == win ? a : b;
+        };
+        const int npro = nloc < S ? nloc : S;
+        for (int r = 0; r < npro; ++r) {
+            const int id = __shfl_sync(0xffffffffu, id_cur, r);
+            if (lane == 0) {
+                issue(&tmk, 0, r, (rr + r) % S, id);
+                issue(&tmv, 1, r, (rr + r) % S, id);
+            }
+        }
+
+        // ---- online-softmax state ---------------------------------------------------
+        // Accumulator layouts (m16n8 fragments): S^T[t][g] with t = lane/4 (+8),
+        // g = nt*8 + (lane%4)*2 (+1); O^T[d][g] with d = mt*16 + lane/4 (+8) and the
+        // same g.  Each thread keeps (m, l) of its two columns g.  With HL (groups of
+        // at most 4) columns 4..7 of the single n-tile carry the BF16 residual of P
+        // for columns 0..3, so one mma per m-tile serves both halves of P.
+        float o[KS][GN][4];
+#pragma unroll
+        for (int a_ = 0; a_ < KS; ++a_)
+#pragma unroll
+            for (int b_ = 0; b_ < GN; ++b_)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) o[a_][b_][c] = 0.f;
+        float m_run[GN][2], l_run[GN][2];
 #pragma unroll
         for (int nt = 0; nt < GN; ++nt)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                const int g = nt * 8 + gq + c;
-                if (g - nt * 8 < GCOLS) {
-                    wm[warp * RT + g] = m_run[nt][c];
-                    wl[warp * RT + g] = l_run[nt][c];
+                m_run[nt][c] = kNegInf;
+                l_run[nt][c] = 0.f;
+            }
+        int fail_r = -1;
+
+        for (int r = 0; r < nloc; ++r) {
+            const int k = (rr + r) % S;
+            const uint32_t par = ((rr + r) / S) & 1;
+            const int rn = r + S;
+            int id_next = -1;
+            if (rn < nloc) {
+                if ((rn >> 5) != win) {
+                    id_cur = id_nxt;
+                    win = rn >> 5;
+                    id_nxt = load_id((win + 1) * 32 + lane);
+                }
+                id_next = id_at(rn);
+            }
+            if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 0]), par)) {
+                fail_r = r;
+                break;
+            }
+            const int gt = my0 + warp + kWarps * r;
+            const int nvalid = min(kTileTokens, tok1 - gt * kTileTokens);
+            const uint32_t kbase = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES);
+            const uint32_t vbase = kbase + TILE_BYTES;
+
+            // S^T = K . q^T, two accumulator chains (even / odd k-steps)
+            float sc[GN][2][4];
+#pragma unroll
+            for (int nt = 0; nt < GN; ++nt)
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) sc[nt][h2][c] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                dev::ldsm_x4(kbase + (ks >> 2) * (kTileTokens * 128) + lmk_off[ks & 3], a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < GN; ++nt) {
+                    uint32_t b0, b1;
+                    dev::ldsm_x2(q_lm + nt * 8 * QST + ks * 32, b0, b1);
+                    dev::mma_bf16_16816(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
                 }
             }
-    }
+            // The K half is read (every lane's ldmatrix result has been consumed by
+            // an mma): refill it with tile r + S.  A read-then-overwrite by the TMA
+            // needs no proxy fence once the read values are in registers.
+            if (rn < nloc) {
+                __syncwarp();
+                if (lane == 0) issue(&tmk, 0, rn, k, id_next);
+            }
+
+            // column softmax over the tile's tokens, base 2, tokens past the range masked
+            float alpha[GN][2];
+            float pv[GN][4];
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
+            for (int nt = 0; nt < GN; ++nt) {
+                float x[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int t = tq + (c >> 1) * 8;
+                    const float v = (sc[nt][0][c] + sc[nt][1][c]) * p.scale_log2;
+                    x[c] = t < nvalid ? v : kNegInf;
+                }
+                float cmx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    cmx[0] = fmaxf(cmx[0], __shfl_xor_sync(0xffffffffu, cmx[0], off));
+                    cmx[1] = fmaxf(cmx[1], __shfl_xor_sync(0xffffffffu, cmx[1], off));
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float m_new = fmaxf(m_run[nt][c], cmx[c]);
+                    alpha[nt][c] = dev::exp2_approx(m_run[nt][c] - m_new);
+                    const float e0 = dev::exp2_approx(x[c] - m_new);
+                    const float e1 = dev::exp2_approx(x[c + 2] - m_new);
+                    pv[nt][c] = e0;
+                    pv[nt][c + 2] = e1;
+                    l_run[nt][c] = l_run[nt][c] * alpha[nt][c] + (e0 + e1);
+                    m_run[nt][c] = m_new;
+                }
+            }
+
+            // P^T as the B operand of O^T += V^T P^T: pack to BF16 (high part and
+            // residual) and transpose each 8x8 block in registers.
+            uint32_t bh[GN][2], bl[GN][2];
+#pragma unroll
+            for (int nt = 0; nt < GN; ++nt)
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const float e0 = pv[nt][2 * h2], e1 = pv[nt][2 * h2 + 1];
+                    const uint32_t hi = dev::pack_bf16x2(e0, e1);
+                    const uint32_t lo = dev::pack_bf16x2(e0 - dev::bf16_lo_f32(hi), e1 - dev::bf16_hi_f32(hi));
+                    bh[nt][h2] = dev::movmatrix_trans(hi);
+                    bl[nt][h2] = dev::movmatrix_trans(lo);
+                }
+            if constexpr (HL) {
+                // lanes 16..31 hold rows g = 4..7 of the transposed blocks: give them
+                // the residual of rows 0..3 instead
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint32_t lo_src = __shfl_sync(0xffffffffu, bl[0][h2], lane & 15);
+                    bh[0][h2] = lane < 16 ? bh[0][h2] : lo_src;
+                }
+            }
+
+            // rescale O^T columns whose max moved (HL: columns 4..7 follow 0..3)
+            bool any = false;
+#pragma unroll
+            for (int nt = 0; nt < GN; ++nt) any |= (alpha[nt][0] != 1.f) | (alpha[nt][1] != 1.f);
+            if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                for (int nt = 0; nt < GN; ++nt) {
+                    float a0 = alpha[nt][0], a1 = alpha[nt][1];
+                    if constexpr (HL) {
+                        const float p0 = __shfl_xor_sync(0xffffffffu, a0, 2);
+                        const float p1 = __shfl_xor_sync(0xffffffffu, a1, 2);
+                        if (lane & 2) {
+                            a0 = p0;
+                            a1 = p1;
+                        }
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        o[mt][nt][0] *= a0;
+                        o[mt][nt][1] *= a1;
+                        o[mt][nt][2] *= a0;
+                        o[mt][nt][3] *= a1;
+                    }
+                }
+            }
+
+            if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 1]), par)) {
+                fail_r = r;
+                break;
+            }
+            // O^T += V^T . P^T  (V rows past the range may hold anything: mask them)
+            auto pv_tile = [&](uint32_t mask01, uint32_t mask89) {
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t a0, a1, a2, a3;
+                    dev::ldsm_x4_trans(vbase + (mt >> 2) * (kTileTokens * 128) + lmv_off[mt & 3], a0, a1, a2, a3);
+                    a0 &= mask01;
+                    a1 &= mask01;
+                    a2 &= mask89;
+                    a3 &= mask89;
+#pragma unroll
+                    for (int nt = 0; nt < GN; ++nt) {
+                        dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                        if constexpr (!HL) dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                    }
+                }
+            };
+            if (nvalid == kTileTokens) {
+                pv_tile(0xffffffffu, 0xffffffffu);
+            } else {
+                const int tv0 = (lane & 3) * 2;
+                pv_tile((tv0 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 1 < nvalid ? 0xffff0000u : 0u),
+                        (tv0 + 8 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 9 < nvalid ? 0xffff0000u : 0u));
+            }
+            // the V half is read: refill it with tile r + S
+            if (rn < nloc) {
+                __syncwarp();
+                if (lane == 0) issue(&tmv, 1, rn, k, id_next);
+            }
+        }
+        if (fail_r >= 0) {
+            // A bounded wait ran out.  Record it and drain (bounded) whatever this
+            // warp may still have in flight before the ring is reused.
+            if (lane == 0) dev::flag_status(p.status, kDevWaitTimeout);
+            const int last = fail_r + S + 1 < nloc ? fail_r + S + 1 : nloc;
+            for (int r = fail_r; r < last; ++r)
+                for (int h = 0; h < 2; ++h)
+                    dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + (rr + r) % S) * 2 + h]),
+                                           ((rr + r) / S) & 1, 100000000ull);
+        }
+        rr += nloc;
+
+        // ---- warp merge of the part (fixed warp order) -----------------------------
+        // column sums over the tokens of all lanes of a column
 #pragma unroll
         for (int nt = 0; nt < GN; ++nt)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int g = nt * 8 + gq + (c & 1);
-                const int d = mt * 16 + tq + (c >> 1) * 8;
-                if (g - nt * 8 < GCOLS) wo[(warp * RT + g) * OSTRIDE + d] = o[mt][nt][c];
-            }
-    __syncthreads();
-
-    // CTA statistics of each valid row: max, warp weights, sum.
-    if (tid < Gt) {
-        float M = kNegInf;
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * RT + tid]);
-        float Lsum = 0.f;
+                for (int off = 4; off < 32; off <<= 1)
+                    l_run[nt][c] += __shfl_xor_sync(0xffffffffu, l_run[nt][c], off);
+        if constexpr (HL) {
+            // columns 0..3 = high part + residual held in columns 4..7
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float mw = wm[w * RT + tid];
-            const float wt = mw == kNegInf ? 0.f : dev::exp2_approx(mw - M);
-            ww[w * RT + tid] = wt;
-            Lsum += wt * wl[w * RT + tid];
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) o[mt][0][c] += __shfl_xor_sync(0xffffffffu, o[mt][0][c], 2);
         }
-        cm[tid] = M;
-        cl[tid] = Lsum;
-    }
-    __syncthreads();
+        __syncthreads();  // every warp is done with the ring; reuse it for the merge
+        if (tq == 0) {
+#pragma unroll
+            for (int nt = 0; nt < GN; ++nt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int g = nt * 8 + gq + c;
+                    if (g - nt * 8 < GCOLS) {
+                        wm[warp * RT + g] = m_run[nt][c];
+                        wl[warp * RT + g] = l_run[nt][c];
+                    }
+                }
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < GN; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int g = nt * 8 + gq + (c & 1);
+                    const int d = mt * 16 + tq + (c >> 1) * 8;
+                    if (g - nt * 8 < GCOLS) wo[(warp * RT + g) * OSTRIDE + d] = o[mt][nt][c];
+                }
+        __syncthreads();
 
-    // ---- the unit's result: rows dealt to the cluster's ranks round-robin ------
-    // Row g of this rank combines the ranks' CTA results in rank order (C == 1:
-    // straight from the warp partials).  For every row the combine yields
-    // (M, L, O[d]); the epilogue then writes the output, the split's partial, or
-    // folds into the tiled running state.
-    cg::cluster_group cluster = cg::this_cluster();
-    float *co = reinterpret_cast<float *>(smem + plan.result);  // [RT][OSTRIDE]
-    if (C > 1) {
+        // part statistics of each valid row: max, warp weights, sum
+        if (tid < Gt) {
+            float M = kNegInf;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * RT + tid]);
+            float Lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = wm[w * RT + tid];
+                const float wt = mw == kNegInf ? 0.f : dev::exp2_approx(mw - M);
+                ww[w * RT + tid] = wt;
+                Lsum += wt * wl[w * RT + tid];
+            }
+            cm[tid] = M;
+            cl[tid] = Lsum;
+        }
+        __syncthreads();
+        // the part's o: warp partials weighted and summed in warp order
         for (int e = tid; e < Gt * DPAD; e += kThreads) {
             const int g = e / DPAD, d = e - g * DPAD;
             float acc = 0.f;
@@ -604,36 +633,64 @@ __global__ void __launch_bounds__(kThreads)
             for (int w = 0; w < kWarps; ++w) acc += ww[w * RT + g] * wo[(w * RT + g) * OSTRIDE + d];
             co[g * OSTRIDE + d] = acc;
         }
+        if (C == 1) {
+            // fold the part into the running result, in part order
+            __syncthreads();
+            if (tid < Gt) {
+                float Mn, fa, fb;
+                fold_factors(rM[tid], cm[tid], Mn, fa, fb);
+                rL[tid] = fold_value(rL[tid], fa, cl[tid], fb);
+                rM[tid] = Mn;
+                fx[tid * 4 + 2] = fa;
+                fx[tid * 4 + 3] = fb;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < RACC; ++i) {
+                const int e = tid + i * kThreads;
+                const int g = e / DPAD, d = e - g * DPAD;
+                if (g < Gt) racc[i] = fold_value(racc[i], fx[g * 4 + 2], co[g * OSTRIDE + d], fx[g * 4 + 3]);
+            }
+            __syncthreads();  // the ring (and co over it) is free for the next part
+        }
+    }
+
+    // ---- the unit's result: rows dealt to the cluster's ranks round-robin ------
+    // Row g of this rank is the left fold, in part order, of the parts' results
+    // (cluster == 1: already folded into the running result).  The epilogue then
+    // writes the output, the split's partial, or folds into the tiled state.
+    cg::cluster_group cluster = cg::this_cluster();
+    if (C > 1) {
         cluster.sync();
+    } else {
+        // the folded o goes to shared memory for the epilogue (the ring is free)
+#pragma unroll
+        for (int i = 0; i < RACC; ++i) {
+            const int e = tid + i * kThreads;
+            const int g = e / DPAD, d = e - g * DPAD;
+            if (g < Gt) co[g * OSTRIDE + d] = racc[i];
+        }
+        __syncthreads();
     }
     const int nmine = Gt > part ? (Gt - part + C - 1) / C : 0;  // rows g = part + i*C
-    // per-row factors: fx[i] = {M, L, a, b}; fr[i][rk] = weight of rank rk
+    // per-row factors: fx[i] = {M, L, a, b} of the epilogue; fr[i] = fold factors
     if (tid < nmine) {
         const int g = part + tid * C;
         float M = kNegInf, Lsum = 0.f;
         if (C > 1) {
-            float mr[kMaxCluster], lr[kMaxCluster];
-#pragma unroll
-            for (int rk = 0; rk < kMaxCluster; ++rk) {
-                if (rk < C) {
-                    mr[rk] = cluster.map_shared_rank(cm, rk)[g];
-                    lr[rk] = cluster.map_shared_rank(cl, rk)[g];
-                }
-            }
-#pragma unroll
-            for (int rk = 0; rk < kMaxCluster; ++rk)
-                if (rk < C) M = fmaxf(M, mr[rk]);
-#pragma unroll
-            for (int rk = 0; rk < kMaxCluster; ++rk) {
-                if (rk < C) {
-                    const float wt = mr[rk] == kNegInf ? 0.f : dev::exp2_approx(mr[rk] - M);
-                    fr[tid * kMaxCluster + rk] = wt;
-                    Lsum += wt * lr[rk];
-                }
+            for (int jj = 0; jj < V; ++jj) {
+                const float mj = cluster.map_shared_rank(cm, jj)[g];
+                const float lj = cluster.map_shared_rank(cl, jj)[g];
+                float Mn, fa, fb;
+                fold_factors(M, mj, Mn, fa, fb);
+                Lsum = fold_value(Lsum, fa, lj, fb);
+                M = Mn;
+                fr[tid * 2 * kMaxParts + 2 * jj + 0] = fa;
+                fr[tid * 2 * kMaxParts + 2 * jj + 1] = fb;
             }
         } else {
-            M = cm[g];
-            Lsum = cl[g];
+            M = rM[g];
+            Lsum = rL[g];
         }
         const long long row = static_cast<long long>(s) * Hq + h0 + g;
         float fa = 0.f, fb = 0.f;
@@ -666,30 +723,28 @@ __global__ void __launch_bounds__(kThreads)
         const int g = part + i * C;
         float acc0 = 0.f, acc1 = 0.f;
         if (C > 1) {
-            float v0[kMaxCluster], v1[kMaxCluster];
+            float v0[kMaxParts], v1[kMaxParts];
 #pragma unroll
-            for (int rk = 0; rk < kMaxCluster; ++rk) {
-                if (rk < C) {
+            for (int jj = 0; jj < kMaxParts; ++jj) {
+                if (jj < V) {
                     const float2 v = *reinterpret_cast<const float2 *>(
-                        cluster.map_shared_rank(co, rk) + g * OSTRIDE + d);
-                    v0[rk] = v.x;
-                    v1[rk] = v.y;
+                        cluster.map_shared_rank(co, jj) + g * OSTRIDE + d);
+                    v0[jj] = v.x;
+                    v1[jj] = v.y;
                 }
             }
 #pragma unroll
-            for (int rk = 0; rk < kMaxCluster; ++rk) {
-                if (rk < C) {
-                    acc0 += fr[i * kMaxCluster + rk] * v0[rk];
-                    acc1 += fr[i * kMaxCluster + rk] * v1[rk];
+            for (int jj = 0; jj < kMaxParts; ++jj) {
+                if (jj < V) {
+                    const float fa = fr[i * 2 * kMaxParts + 2 * jj + 0];
+                    const float fb = fr[i * 2 * kMaxParts + 2 * jj + 1];
+                    acc0 = fold_value(acc0, fa, v0[jj], fb);
+                    acc1 = fold_value(acc1, fa, v1[jj], fb);
                 }
             }
         } else {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float wt = ww[w * RT + g];
-                acc0 += wt * wo[(w * RT + g) * OSTRIDE + d];
-                acc1 += wt * wo[(w * RT + g) * OSTRIDE + d + 1];
-            }
+            acc0 = co[g * OSTRIDE + d];
+            acc1 = co[g * OSTRIDE + d + 1];
         }
         const long long row = static_cast<long long>(s) * Hq + h0 + g;
         if constexpr (MODE == kModePaged) {

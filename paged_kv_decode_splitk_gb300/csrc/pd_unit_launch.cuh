@@ -11,25 +11,56 @@ namespace pd {
 int unit_smem_bytes(int dpad, int rows, int stages);
 
 template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
-cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p,
-                        int grid_x, int smem_bytes, cudaStream_t stream) {
+cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p_in,
+                        long long units, int smem_bytes, cudaStream_t stream, int layout) {
     auto kern = unit_kernel<DPAD, GN, HL, MODE, PACKED>;
     // Raise the kernel's dynamic shared-memory limit once per device (and
-    // again only if a launch asks for more).
+    // again only if a launch asks for more); remember the SM count and how
+    // many CTAs of this kernel fit on one SM at that size.
     static std::mutex mu;
     static int configured[64] = {0};
+    static int per_sm[64] = {0};
+    static int sm_count[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    int slots = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (configured[dev] < smem_bytes) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (configured[dev] != smem_bytes) {
+            if (configured[dev] < smem_bytes) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+                if (e != cudaSuccess) return e;
+            }
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem_bytes);
             if (e != cudaSuccess) return e;
-            configured[dev] = smem_bytes;
+            if (!sm_count[dev]) {
+                e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+                if (e != cudaSuccess) return e;
+            }
+            per_sm[dev] = n;
+            if (configured[dev] < smem_bytes) configured[dev] = smem_bytes;
         }
+        slots = per_sm[dev] * sm_count[dev];
     }
+    // Where the parts of a unit run.  Both layouts fold the same parts in the
+    // same order, so the choice changes timing only, never the output bits:
+    // when one CTA per part still fits in about one wave, a cluster of
+    // max_parts CTAs per unit (fills the GPU when units are few); otherwise
+    // one CTA per unit walking its parts in sequence.
+    UnitParams p = p_in;
+    int C = 1;
+    if (p.max_parts > 1) {
+        if (layout == 2)
+            C = p.max_parts;
+        else if (layout == 0 && units * p.max_parts * 4 <= static_cast<long long>(slots) * 5)
+            C = p.max_parts;
+    }
+    p.cluster = C;
+    const long long grid_x = units * C;
+    if (grid_x > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_x));
     cfg.blockDim = dim3(kThreads);
@@ -58,4 +89,5 @@ cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const Un
 
 #define PD_INSTANTIATE_UNIT(DPAD, GN, HL, MODE, PACKED)                                      \
     template cudaError_t pd::launch_unit<DPAD, GN, HL, MODE, PACKED>(                        \
-        const CUtensorMap &, const CUtensorMap &, const pd::UnitParams &, int, int, cudaStream_t);
+        const CUtensorMap &, const CUtensorMap &, const pd::UnitParams &, long long, int,       \
+        cudaStream_t, int);

@@ -134,3 +134,26 @@ def test_tiled_sequence_is_batch_invariant(cuda_device):
                           blocks_per_seq=tw.blocks_per_seq[[s]])
     alone = api.bf16_bits(api.run_tiled(api.TiledInputs(one, cuda_device)))
     assert np.array_equal(alone[0], full[s])
+
+
+@pytest.mark.parametrize("kind", ["splitk", "packed", "tiled"])
+def test_part_layout_does_not_change_bits(cuda_device, kind):
+    """A unit's range is cut into parts by its own length and the parts fold in a
+    fixed order; whether they run in one CTA or one per CTA of a cluster (the
+    launch picks from occupancy, so from the batch) must not change a bit."""
+    outs = []
+    try:
+        for layout in (1, 2):
+            pd.pd_debug_set_tuning(0, layout, -1)
+            if kind == "tiled":
+                tw = W.tiled(num_seqs=8, max_blocks=256, seed=3)
+                outs.append(api.bf16_bits(api.run_tiled(api.TiledInputs(tw, cuda_device))))
+            elif kind == "packed":
+                w = W.custom([4096, 700, 33, 2500], 16, 2, 256, seed=72)
+                outs.append(_bits(w, cuda_device, 1, pack=True))
+            else:
+                w = W.custom([5000, 3000, 17, 2600], 24, 8, 128, seed=71)
+                outs.append(_bits(w, cuda_device, 3))
+    finally:
+        pd.pd_debug_set_tuning(0, 0, -1)
+    assert np.array_equal(outs[0], outs[1])
