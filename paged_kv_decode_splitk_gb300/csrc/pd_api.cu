@@ -236,13 +236,17 @@ int default_stages(int dpad) {
 // Longest-first service order for small batches (a scheduling choice only).
 int default_lpt(int num_seqs) {
     const int on = g_debug_lpt >= 0 ? g_debug_lpt : 1;
-    return on && num_seqs <= pd::kLptMaxSeqs ? 1 : 0;
+    return on && num_seqs > 1 && num_seqs <= pd::kLptMaxSeqs ? 1 : 0;
 }
 
 // A unit's range (one split of a sequence, or one tile of it) is cut into up
 // to max_parts parts of about kPartTiles 16-token tiles, by its own length; the
 // parts fold in order.  Build constants: they fix the summation order.
 constexpr int kPartTiles = 32;
+// Bytes of K/V at the start of its part that a paged-mode CTA prefetches into
+// L2 before it waits for the previous kernel (a scheduling hint: it changes no
+// result); a 16-token K+V tile holds 64 * dpad bytes.
+constexpr int kPrefetchBytes = 128 * 1024;
 int max_parts_for(int dpad, bool tiled) { return tiled ? 2 : (dpad >= 256 ? 6 : 4); }
 
 int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
@@ -552,6 +556,7 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = default_lpt(num_seqs);
+    p.prefetch_tiles = kPrefetchBytes / (64 * dpad);
     p.tok_dim = tok_dim;
     p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
     p.status = status;
@@ -769,6 +774,7 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = 0;
+    p.prefetch_tiles = 0;
     p.tok_dim = tok_dim;
     // step_tile carries no scale: 1/sqrt(head_dim), rounded to FP32 first.
     const float inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.head_dim)));

@@ -70,6 +70,7 @@ struct UnitParams {
     int part_tiles;   // tiles per part the cut aims for
     int stages;       // pipeline stages per warp
     int lpt;          // paged mode: serve sequences longest first (needs num_seqs <= kLptMaxSeqs)
+    int prefetch_tiles;  // paged mode: first tiles of the CTA's part prefetched into L2 before the wait
     int tok_dim;      // tensor-map dimension of the token coordinate (1 or 2)
     float scale_log2; // softmax scale * log2(e)
     unsigned int *status;  // device status word (PD_DEV_* flags)

@@ -11,73 +11,84 @@ namespace pd {
 namespace {
 
 constexpr int kMergeWarps = 8;
+constexpr int kMergeCols = 128;   // columns of a row one warp merges (4 per lane)
+constexpr int kMergeBatch = 16;   // splits whose partials are loaded together
 
 // Merge pass (Module attn_splitk page: the split-K workspace of [o, m, l]
-// slots and the non-associative merge).  One warp per (sequence, q head)
-// folds the non-empty splits in split order with the online rule
+// slots and the non-associative merge).  One warp per (sequence, q head, 128
+// columns) folds the non-empty splits in split order with the online rule
 //   M' = max(M, m_i),  L = L 2^(M - M') + l_i 2^(m_i - M'),  O likewise,
-// and writes out = O / L as BF16 (0 when L is 0).  All loads of a row are
-// independent of the arithmetic, so they are issued together.  Sequences with
-// at most one non-empty split were written by the partial pass directly and
-// are skipped here.
+// and writes out = O / L as BF16 (0 when L is 0).  The partials of up to 16
+// splits and the context length are loaded in one go, before the length says
+// which splits are non-empty (every slot of the workspace is in bounds; slots
+// past the non-empty splits are read and ignored), so the pass costs one
+// round trip to memory.  Sequences with at most one non-empty split were
+// written by the partial pass directly and are left alone here.
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_constant__ MergeParams p) {
     const float kNegInf = -__int_as_float(0x7f800000);
     dev::griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
-    if (row >= static_cast<long long>(p.num_seqs) * p.num_q_heads) return;
+    const int D = p.head_dim;
+    const int N = p.num_splits;
+    const int chunks = (D + kMergeCols - 1) / kMergeCols;
+    const long long item = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
+    if (item >= static_cast<long long>(p.num_seqs) * p.num_q_heads * chunks) return;
+    const long long row = item / chunks;
+    const int d0 = static_cast<int>(item - row * chunks) * kMergeCols + lane * 4;
+    const bool cols = d0 < D;  // D is a multiple of 8: the lane's 4 columns are all in range
+    // Wait before any global read: the partial pass may have started before the
+    // kernel ahead of it (which may write context_lens) finished, and waiting
+    // for the partial pass's completion covers that kernel too.
+    dev::griddep_wait();
     const int s = static_cast<int>(row / p.num_q_heads);
     int L = p.context_lens[s];
-    L = L < 0 ? 0 : (L > p.max_tokens ? p.max_tokens : L);
-    const int chunk = split_chunk_tokens(L, p.num_splits, p.block_size, p.min_kv_per_split);
-    const int nsu = splits_used(L, chunk);
-    if (nsu <= 1) return;
-    dev::griddep_wait();  // the partial pass's workspace is complete and visible
+    const float *ml = p.ws_ml + row * N * 2;
+    const float *ob = p.ws_o + row * N * D + d0;
 
-    const float *ml = p.ws_ml + row * p.num_splits * 2;
-    const int D = p.head_dim;
-    for (int d0 = lane * 4; d0 < D; d0 += 128) {
-        float M = kNegInf, Lsum = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        constexpr int kBatch = 4;
-        for (int i0 = 0; i0 < nsu; i0 += kBatch) {
-            float mi[kBatch], li[kBatch];
-            float4 oi[kBatch];
+    float M = kNegInf, Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int nsu = -1;
+    for (int i0 = 0; i0 < N; i0 += kMergeBatch) {
+        float4 oi[kMergeBatch];
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const int i = i0 + j;
-                if (i < nsu) {
-                    const float2 v = *reinterpret_cast<const float2 *>(ml + 2 * i);
-                    mi[j] = v.x;
-                    li[j] = v.y;
-                    oi[j] = *reinterpret_cast<const float4 *>(p.ws_o + (row * p.num_splits + i) * D + d0);
-                }
-            }
+        for (int j = 0; j < kMergeBatch; ++j)
+            oi[j] = (cols && i0 + j < N) ? *reinterpret_cast<const float4 *>(ob + static_cast<long long>(i0 + j) * D)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        // lane j holds (m, l) of split i0 + j
+        float2 mlj = make_float2(kNegInf, 0.f);
+        if (lane < kMergeBatch && i0 + lane < N) mlj = *reinterpret_cast<const float2 *>(ml + 2 * (i0 + lane));
+        if (nsu < 0) {
+            L = L < 0 ? 0 : (L > p.max_tokens ? p.max_tokens : L);
+            nsu = splits_used(L, split_chunk_tokens(L, N, p.block_size, p.min_kv_per_split));
+        }
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                if (i0 + j < nsu && mi[j] != kNegInf) {
-                    const float Mn = fmaxf(M, mi[j]);
-                    const float a = M == kNegInf ? 0.f : dev::exp2_approx(M - Mn);
-                    const float b = dev::exp2_approx(mi[j] - Mn);
-                    Lsum = Lsum * a + li[j] * b;
-                    acc.x = acc.x * a + oi[j].x * b;
-                    acc.y = acc.y * a + oi[j].y * b;
-                    acc.z = acc.z * a + oi[j].z * b;
-                    acc.w = acc.w * a + oi[j].w * b;
-                    M = Mn;
-                }
+        for (int j = 0; j < kMergeBatch; ++j) {
+            const float mi = __shfl_sync(0xffffffffu, mlj.x, j);
+            const float li = __shfl_sync(0xffffffffu, mlj.y, j);
+            if (i0 + j < nsu && mi != kNegInf) {
+                const float Mn = fmaxf(M, mi);
+                const float a = M == kNegInf ? 0.f : dev::exp2_approx(M - Mn);
+                const float b = dev::exp2_approx(mi - Mn);
+                Lsum = Lsum * a + li * b;
+                acc.x = acc.x * a + oi[j].x * b;
+                acc.y = acc.y * a + oi[j].y * b;
+                acc.z = acc.z * a + oi[j].z * b;
+                acc.w = acc.w * a + oi[j].w * b;
+                M = Mn;
             }
         }
-        const bool pos = Lsum > 0.f;
-        __nv_bfloat162 lo = __floats2bfloat162_rn(pos ? __fdiv_rn(acc.x, Lsum) : 0.f,
-                                                  pos ? __fdiv_rn(acc.y, Lsum) : 0.f);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(pos ? __fdiv_rn(acc.z, Lsum) : 0.f,
-                                                  pos ? __fdiv_rn(acc.w, Lsum) : 0.f);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t *>(&lo);
-        pk.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(p.out + row * D + d0) = pk;
+        if (i0 + kMergeBatch >= nsu) break;  // the rest are empty splits
     }
+    if (nsu <= 1 || !cols) return;
+    const bool pos = Lsum > 0.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(pos ? __fdiv_rn(acc.x, Lsum) : 0.f,
+                                              pos ? __fdiv_rn(acc.y, Lsum) : 0.f);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(pos ? __fdiv_rn(acc.z, Lsum) : 0.f,
+                                              pos ? __fdiv_rn(acc.w, Lsum) : 0.f);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p.out + row * D + d0) = pk;
 }
 
 // TiledAttention::begin_step: (m, l, o) <- (-inf, 0, 0) over `rows` rows.
@@ -116,10 +127,11 @@ int grid_for(long long n, int threads) {
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream, bool programmatic) {
-    const long long rows = static_cast<long long>(p.num_seqs) * p.num_q_heads;
-    if (rows == 0) return cudaSuccess;
+    const long long items = static_cast<long long>(p.num_seqs) * p.num_q_heads *
+                            ((p.head_dim + kMergeCols - 1) / kMergeCols);
+    if (items == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps));
+    cfg.gridDim = dim3(static_cast<unsigned>((items + kMergeWarps - 1) / kMergeWarps));
     cfg.blockDim = dim3(kMergeWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -80,7 +80,7 @@ struct UnitSmem {
     int result;  // CTA result o [rows][dpad+4], read by the cluster peers: overlaps the ring
     int qs;      // the CTA's query rows, BF16, padded rows
     int stats;   // per-warp m, l, weights; part m, l; row factors; fold factors; running m, l
-    int bars;    // two mbarriers (K, V) per stage
+    int bars;    // two mbarriers (K, V) per stage, then the cluster's ready and done barriers
     int lpt;     // longest-first order: context lengths + the pick
     int total;   // bytes to request, including the alignment slack
 };
@@ -104,7 +104,7 @@ __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stage
     s.qs = (end + 15) / 16 * 16;
     s.stats = s.qs + rows * (dpad * 2 + 16);
     s.bars = s.stats + (unit_stat_floats(rows) * 4 + 15) / 16 * 16;
-    s.lpt = s.bars + kWarps * stages_per_warp * 2 * 8;
+    s.lpt = s.bars + (kWarps * stages_per_warp * 2 + 2) * 8;
     s.total = 1024 /* alignment slack */ + s.lpt + (kLptMaxSeqs + 4) * 4;
     return s;
 }
@@ -124,17 +124,18 @@ __global__ void __launch_bounds__(kThreads)
     static_assert(QPT * kThreads == RT * (DPAD / 2), "q staging must divide evenly");
     const float kNegInf = -__int_as_float(0x7f800000);
 
-    // Programmatic dependent launch: let the next kernel in the stream start
-    // its launch now; it waits (griddepcontrol.wait) for this grid to finish
-    // before it touches memory.
-    dev::griddep_launch_dependents();
-
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int S = p.stages;
     const UnitSmem plan = unit_smem_plan(DPAD, RT, S);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + plan.bars);  // [kWarps*S][K, V]
+    // Cluster hand-off (one phase each): `ready` of a row owner completes when
+    // every active rank has published its part; `done` of an active rank when
+    // every owner has finished reading it.  Both expect kMaxParts arrivals; a
+    // CTA arrives for the ranks that will not.
+    uint64_t *bar_ready = bars + 2 * kWarps * p.stages;
+    uint64_t *bar_done = bar_ready + 1;
     uint8_t *ring = smem + plan.stages;
     uint8_t *qsm = smem + plan.qs;
     float *stats = reinterpret_cast<float *>(smem + plan.stats);
@@ -149,11 +150,16 @@ __global__ void __launch_bounds__(kThreads)
         dev::prefetch_tensormap(&tmk);
         dev::prefetch_tensormap(&tmv);
         for (int i = 0; i < 2 * kWarps * S; ++i) dev::mbar_init(dev::smem_addr(&bars[i]), 1);
+        dev::mbar_init(dev::smem_addr(bar_ready), kMaxParts);
+        dev::mbar_init(dev::smem_addr(bar_done), kMaxParts);
         dev::fence_mbar_init();
     }
-    dev::griddep_wait();  // the previous kernel's writes (q, caches, tables, out) are visible
+    // Every rank of a cluster arrives here, so a rank may leave early (an idle
+    // rank, an empty unit) without holding the others; ranks that signal peers
+    // wait on this barrier first, which makes the initialisations visible.
+    if (p.cluster > 1) dev::cluster_arrive_relaxed();
 
-    // ---- which unit ---------------------------------------------------------
+    // ---- which unit (launch geometry only) ------------------------------------
     const int C = p.cluster;
     const int part = blockIdx.x % C;
     int u = blockIdx.x / C;
@@ -166,34 +172,86 @@ __global__ void __launch_bounds__(kThreads)
     u /= p.qtiles;
     const int kvh = u % p.num_kv_heads;
     int s = u / p.num_kv_heads;
-    if constexpr (MODE == kModePaged) {
-        if (p.lpt) {
-            // Serve the s-th longest sequence (ties by index), so that the
-            // longest units start first.  Only which CTA serves a sequence
-            // changes; its arithmetic does not.
-            int *lens_s = reinterpret_cast<int *>(smem + plan.lpt);
-            int &pick_s = lens_s[kLptMaxSeqs];
-            const int ns = p.num_seqs;
-            const int Lmax = p.max_blocks_per_seq * p.block_size;
-            for (int c = tid; c < ns; c += kThreads) {
-                const int Lc = p.context_lens[c];
-                lens_s[c] = Lc < 0 ? 0 : (Lc > Lmax ? Lmax : Lc);
-            }
-            __syncthreads();
-            for (int c = tid; c < ns; c += kThreads) {
-                const int Lc = lens_s[c];
-                int rank = 0;
-                for (int j = 0; j < ns; ++j) rank += (lens_s[j] > Lc) || (lens_s[j] == Lc && j < c);
-                if (rank == s) pick_s = c;
-            }
-            __syncthreads();
-            s = pick_s;
+    const int bs = p.block_size;
+    const int Lmax = p.max_blocks_per_seq * bs;
+    const int tiles_per_block = bs / kTileTokens;
+
+    // The s-th longest sequence (ties by index), so that the longest units
+    // start first.  Only which CTA serves a sequence changes; its arithmetic
+    // does not.  `spec`: lengths read through L2 only, before the wait.
+    auto longest_first = [&](bool spec) -> int {
+        int *lens_s = reinterpret_cast<int *>(smem + plan.lpt);
+        int &pick_s = lens_s[kLptMaxSeqs];
+        const int ns = p.num_seqs;
+        for (int c = tid; c < ns; c += kThreads) {
+            const int Lc = spec ? __ldcg(p.context_lens + c) : p.context_lens[c];
+            lens_s[c] = Lc < 0 ? 0 : (Lc > Lmax ? Lmax : Lc);
         }
+        __syncthreads();
+        for (int c = tid; c < ns; c += kThreads) {
+            const int Lc = lens_s[c];
+            int rank = 0;
+            for (int j = 0; j < ns; ++j) rank += (lens_s[j] > Lc) || (lens_s[j] == Lc && j < c);
+            if (rank == s) pick_s = c;
+        }
+        __syncthreads();
+        const int picked = pick_s;
+        __syncthreads();  // lens_s may be rewritten by the next call
+        return picked;
+    };
+
+    // ---- speculative L2 prefetch, before the wait ------------------------------
+    // The previous kernel in the stream may still be writing the lengths, the
+    // block table or the caches, so nothing read here is used for results:
+    // lengths and block ids are read through L2 only (no stale L1 line is left
+    // behind), and they only choose which of this CTA's first tiles to prefetch
+    // into L2 (a prefetch reads no value; L2 is where writes land, so a line
+    // prefetched early is never stale).  Everything is read again after the
+    // wait.  This fills the DRAM idle time at the previous kernel's tail.
+    if constexpr (MODE == kModePaged) {
+        if (p.prefetch_tiles > 0) {
+            const int ss = p.lpt ? longest_first(true) : s;
+            int L = __ldcg(p.context_lens + ss);
+            L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
+            const int chunk = split_chunk_tokens(L, p.num_splits, bs, p.min_kv_per_split);
+            const long long a = static_cast<long long>(split) * chunk;
+            const int t0 = static_cast<int>(a < L ? a : L);
+            const int t1 = static_cast<int>(a + chunk < L ? a + chunk : L);
+            if (t0 < t1) {
+                const int tile0 = t0 / kTileTokens;
+                const int ntiles = (t1 + kTileTokens - 1) / kTileTokens - tile0;
+                const int V = max(1, min(p.max_parts, (ntiles + p.part_tiles - 1) / p.part_tiles));
+                const int j = C == 1 ? 0 : part;
+                if (j < V) {
+                    const int my0 = tile0 + (j * ntiles) / V;
+                    const int n = min(tile0 + ((j + 1) * ntiles) / V - my0, p.prefetch_tiles);
+                    const int32_t *ids = p.block_table + static_cast<long long>(ss) * p.max_blocks_per_seq;
+                    for (int t = tid; t < n; t += kThreads) {
+                        const int gt = my0 + t;
+                        const int id = __ldcg(ids + gt / tiles_per_block);
+                        if (id >= 0 && id < p.num_blocks) {
+                            const int sub = (gt % tiles_per_block) * kTileTokens;
+                            const int c1 = p.tok_dim == 1 ? sub : kvh;
+                            const int c2 = p.tok_dim == 1 ? kvh : sub;
+#pragma unroll
+                            for (int b = 0; b < NBOX; ++b) {
+                                dev::tma_prefetch_4d(&tmk, b * kBoxCols, c1, c2, id);
+                                dev::tma_prefetch_4d(&tmv, b * kBoxCols, c1, c2, id);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    dev::griddep_wait();  // the previous kernel's writes (q, caches, tables, out) are visible
+    if constexpr (MODE == kModePaged) {
+        if (p.lpt) s = longest_first(false);
     }
     const int G = PACKED ? PD_GQA : p.group;
     const int D = PACKED ? PD_HDIM : p.head_dim;
     const int Hq = PACKED ? p.num_kv_heads * PD_GQA : p.num_q_heads;
-    const int bs = p.block_size;
     const int g0 = qt * RT;                       // first group row of this CTA
     const int Gt = min(RT, G - g0);               // valid rows
     const int h0 = kvh * G + g0;                  // first query head
@@ -219,7 +277,6 @@ __global__ void __launch_bounds__(kThreads)
     const int32_t *ids_base;
     if constexpr (MODE == kModePaged) {
         int L = p.context_lens[s];
-        const int Lmax = p.max_blocks_per_seq * bs;
         if (L < 0 || L > Lmax) {
             if (tid == 0 && part == 0 && split == 0 && qt == 0 && kvh == 0)
                 dev::flag_status(p.status, kDevBadContextLen);
@@ -262,6 +319,9 @@ __global__ void __launch_bounds__(kThreads)
     const int tile0 = tok0 / kTileTokens;
     const int ntiles = (tok1 + kTileTokens - 1) / kTileTokens - tile0;
     const int V = max(1, min(p.max_parts, (ntiles + p.part_tiles - 1) / p.part_tiles));
+    // A rank of a cluster beyond the unit's parts has nothing to do: no peer
+    // reads or signals it, so it leaves now and frees its slot.
+    if (C > 1 && part >= V) return;
 
     // ---- q to shared memory (the barriers were initialised at the start) ----------
 #pragma unroll
@@ -287,7 +347,6 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
 
     const uint64_t policy = dev::l2_evict_first_policy();
-    const int tiles_per_block = bs / kTileTokens;
 
     // B operand of S^T = K q^T (q^T: d x g), one x2 ldmatrix per k-step and
     // n-tile: lanes 0-7 address rows g of columns k0..k0+7, lanes 8-15 k0+8..15.
@@ -655,13 +714,44 @@ __global__ void __launch_bounds__(kThreads)
         }
     }
 
-    // ---- the unit's result: rows dealt to the cluster's ranks round-robin ------
-    // Row g of this rank is the left fold, in part order, of the parts' results
-    // (cluster == 1: already folded into the running result).  The epilogue then
-    // writes the output, the split's partial, or folds into the tiled state.
+    // Programmatic dependent launch: the next kernel in the stream may start
+    // launching once every CTA of this grid has streamed its tiles (it waits,
+    // with griddepcontrol.wait, for this grid to finish before it uses any
+    // memory).  Triggering here rather than at the start lets its CTAs take
+    // the SMs this grid is leaving, in launch order, instead of whatever slots
+    // happen to be free early.
+    dev::griddep_launch_dependents();
+
+    // ---- the unit's result: rows dealt to the active ranks round-robin --------
+    // Row g is owned by rank g % V and is the left fold, in part order, of the
+    // parts' results (cluster == 1: already folded into the running result).
+    // The epilogue then writes the output, the split's partial, or folds into
+    // the tiled state.
+    // When every rank of the cluster holds a part, the hand-offs are the
+    // hardware cluster barrier; otherwise the idle ranks have left and the
+    // active ones hand off through the ready / done mbarriers.
     cg::cluster_group cluster = cg::this_cluster();
-    if (C > 1) {
-        cluster.sync();
+    const int RK = C > 1 ? V : 1;                  // ranks rows are dealt to
+    const int nown = C > 1 ? min(V, Gt) : 1;       // ranks that own a row
+    const bool full = C > 1 && V == C;
+    if (full) {
+        dev::cluster_wait();  // (the arrive at the start)
+        cluster.sync();       // every part is published
+    } else if (C > 1) {
+        dev::cluster_wait();  // the peers' barriers are initialised
+        __syncthreads();      // this part's co, cm and cl are complete
+        if (tid == 0) {
+            // release at cluster scope: the CTA's writes above (ordered before
+            // this thread by the barrier) are visible to an owner that acquires
+            for (int r = 0; r < nown; ++r)
+                dev::mbar_arrive_cluster(dev::map_to_rank(dev::smem_addr(bar_ready), r));
+            if (part < nown && V < kMaxParts) dev::mbar_arrive_count(dev::smem_addr(bar_ready), kMaxParts - V);
+            if (nown < kMaxParts) dev::mbar_arrive_count(dev::smem_addr(bar_done), kMaxParts - nown);
+        }
+        if (part < nown) {
+            if (!dev::mbar_wait_cluster_bounded(dev::smem_addr(bar_ready), 0) && tid == 0)
+                dev::flag_status(p.status, kDevWaitTimeout);
+        }
     } else {
         // the folded o goes to shared memory for the epilogue (the ring is free)
 #pragma unroll
@@ -672,10 +762,10 @@ __global__ void __launch_bounds__(kThreads)
         }
         __syncthreads();
     }
-    const int nmine = Gt > part ? (Gt - part + C - 1) / C : 0;  // rows g = part + i*C
+    const int nmine = Gt > part ? (Gt - part + RK - 1) / RK : 0;  // rows g = part + i*RK
     // per-row factors: fx[i] = {M, L, a, b} of the epilogue; fr[i] = fold factors
     if (tid < nmine) {
-        const int g = part + tid * C;
+        const int g = part + tid * RK;
         float M = kNegInf, Lsum = 0.f;
         if (C > 1) {
             for (int jj = 0; jj < V; ++jj) {
@@ -720,7 +810,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int e = tid; e < nmine * halfD; e += kThreads) {
         const int i = e / halfD;
         const int d = (e - i * halfD) * 2;
-        const int g = part + i * C;
+        const int g = part + i * RK;
         float acc0 = 0.f, acc1 = 0.f;
         if (C > 1) {
             float v0[kMaxParts], v1[kMaxParts];
@@ -767,7 +857,21 @@ __global__ void __launch_bounds__(kThreads)
             *so = cur;
         }
     }
-    if (C > 1) cluster.sync();  // peers keep their shared memory until every rank has read it
+    if (full) {
+        cluster.sync();  // peers keep their shared memory until every rank has read it
+    } else if (C > 1) {
+        // Tell every active rank that this owner has read it (relaxed: the
+        // reads have returned, and the output stores need not drain first);
+        // keep this CTA's shared memory alive until its own readers are done.
+        __syncthreads();
+        if (tid == 0) {
+            if (part < nown)
+                for (int r = 0; r < V; ++r)
+                    dev::mbar_arrive_cluster_relaxed(dev::map_to_rank(dev::smem_addr(bar_done), r));
+            if (!dev::mbar_wait_cluster_bounded(dev::smem_addr(bar_done), 0))
+                dev::flag_status(p.status, kDevWaitTimeout);
+        }
+    }
 }
 
 }  // namespace pd

@@ -61,6 +61,10 @@ cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const Un
     p.cluster = C;
     const long long grid_x = units * C;
     if (grid_x > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // The early L2 prefetch pays off only for CTAs that are resident while the
+    // previous kernel drains, i.e. a grid that fits in one wave; CTAs of later
+    // waves would just read the lengths and the block table twice.
+    if (grid_x > slots) p.prefetch_tiles = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_x));
     cfg.blockDim = dim3(kThreads);
