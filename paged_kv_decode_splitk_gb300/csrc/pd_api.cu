@@ -219,18 +219,23 @@ int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int
 }
 
 // ---- launch choices ----------------------------------------------------------------
-// Stages per warp of the unit pipeline: about 64 KB of K/V in flight per CTA
-// so that two or three CTAs share an SM.
+// Stages per warp of the unit pipeline.  A single-wave launch keeps about
+// 32-64 KB of K/V in flight per CTA so that three or four CTAs share an SM; a
+// launch of several waves of one-CTA units (each unit short, its start-up
+// latency exposed) doubles the ring at head dims up to 128, measured ~3%
+// faster on the large-batch workload at D = 128.
 int g_debug_stages = 0;
 int g_debug_cluster = 0;
 int g_debug_lpt = -1;
 
 int default_stages(int dpad) {
     if (g_debug_stages > 0) return g_debug_stages;
-    switch (dpad) {
-        case 64: return 2;
-        default: return 1;
-    }
+    return dpad <= 64 ? 2 : 1;
+}
+
+int default_stages_seq(int dpad) {
+    if (g_debug_stages > 0) return g_debug_stages;
+    return dpad <= 128 ? 2 : 1;
 }
 
 // Longest-first service order for small batches (a scheduling choice only).
@@ -247,22 +252,22 @@ constexpr int kPartTiles = 32;
 // L2 before it waits for the previous kernel (a scheduling hint: it changes no
 // result); a 16-token K+V tile holds 64 * dpad bytes.
 constexpr int kPrefetchBytes = 128 * 1024;
-int max_parts_for(int dpad, bool tiled) { return tiled ? 2 : (dpad >= 256 ? 6 : 4); }
+int max_parts_for(int dpad, bool tiled) { return tiled ? 2 : (dpad >= 256 ? 8 : 4); }
 
 int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
 
 template <int MODE>
 cudaError_t dispatch_unit(int dpad, int gn, bool hl, bool packed, const CUtensorMap &tk,
-                          const CUtensorMap &tv, const pd::UnitParams &p, long long units, int smem,
-                          cudaStream_t st) {
+                          const CUtensorMap &tv, const pd::UnitParams &p, long long units,
+                          int stages_seq, cudaStream_t st) {
     using namespace pd;
     const int layout = g_debug_cluster == 1 ? 1 : (g_debug_cluster > 1 ? 2 : 0);
-    if (packed) return launch_unit<256, 1, false, kModePaged, true>(tk, tv, p, units, smem, st, layout);
+    if (packed) return launch_unit<256, 1, false, kModePaged, true>(tk, tv, p, units, stages_seq, st, layout);
 #define PD_DISPATCH_D(DP)                                                                          \
     if (dpad == DP) {                                                                              \
-        if (gn == 2) return launch_unit<DP, 2, false, MODE, false>(tk, tv, p, units, smem, st, layout); \
-        if (hl) return launch_unit<DP, 1, true, MODE, false>(tk, tv, p, units, smem, st, layout);       \
-        return launch_unit<DP, 1, false, MODE, false>(tk, tv, p, units, smem, st, layout);              \
+        if (gn == 2) return launch_unit<DP, 2, false, MODE, false>(tk, tv, p, units, stages_seq, st, layout); \
+        if (hl) return launch_unit<DP, 1, true, MODE, false>(tk, tv, p, units, stages_seq, st, layout);       \
+        return launch_unit<DP, 1, false, MODE, false>(tk, tv, p, units, stages_seq, st, layout);              \
     }
     PD_DISPATCH_D(64)
     PD_DISPATCH_D(128)
@@ -566,8 +571,10 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     if (smem > max_smem_optin())
         return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
                     smem, max_smem_optin());
+    int stages_seq = default_stages_seq(dpad);
+    if (pd::unit_smem_bytes(dpad, rows, stages_seq) > max_smem_optin()) stages_seq = stages;
     cudaError_t e = dispatch_unit<pd::kModePaged>(dpad, gn, !packed && G <= 4, packed, tk, tv, p, units,
-                                                  smem, st);
+                                                  stages_seq, st);
     if (e != cudaSuccess) return cuda_fail(e, "unit kernel launch");
     if (num_splits > 1) {
         pd::MergeParams mp = {};
@@ -774,6 +781,8 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = 0;
+    // No early prefetch in the tiled step: measured no gain (the begin pass or
+    // the previous step ahead of it leaves no idle tail to fill).
     p.prefetch_tiles = 0;
     p.tok_dim = tok_dim;
     // step_tile carries no scale: 1/sqrt(head_dim), rounded to FP32 first.
@@ -784,7 +793,9 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     if (smem > max_smem_optin())
         return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
                     smem, max_smem_optin());
-    cudaError_t e = dispatch_unit<pd::kModeTiled>(dpad, gn, G <= 4, false, tk, tv, p, units, smem,
+    int stages_seq = default_stages_seq(dpad);
+    if (pd::unit_smem_bytes(dpad, rows, stages_seq) > max_smem_optin()) stages_seq = stages;
+    cudaError_t e = dispatch_unit<pd::kModeTiled>(dpad, gn, G <= 4, false, tk, tv, p, units, stages_seq,
                                                   static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tiled step launch");
     return ok();

@@ -70,7 +70,7 @@ struct UnitParams {
     int part_tiles;   // tiles per part the cut aims for
     int stages;       // pipeline stages per warp
     int lpt;          // paged mode: serve sequences longest first (needs num_seqs <= kLptMaxSeqs)
-    int prefetch_tiles;  // paged mode: first tiles of the CTA's part prefetched into L2 before the wait
+    int prefetch_tiles;  // first tiles of the CTA's part prefetched into L2 before the wait (0: none)
     int tok_dim;      // tensor-map dimension of the token coordinate (1 or 2)
     float scale_log2; // softmax scale * log2(e)
     unsigned int *status;  // device status word (PD_DEV_* flags)
@@ -93,9 +93,11 @@ int unit_smem_bytes(int dpad, int rows, int stages);
 
 // Kernel launchers (defined in the per-head-dim translation units).
 // layout: 0 = choose from occupancy, 1 = one CTA per unit, 2 = one CTA per part.
+// p.stages is the ring depth per warp of a single-wave launch, stages_seq that
+// of a launch of several waves of one-CTA units (both must fit the device).
 template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
 cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p,
-                        long long units, int smem_bytes, cudaStream_t stream, int layout);
+                        long long units, int stages_seq, cudaStream_t stream, int layout);
 
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream, bool programmatic);
 cudaError_t launch_tiled_begin(float *m, float *l, float *o, int rows, int head_dim,

@@ -207,37 +207,46 @@ __global__ void __launch_bounds__(kThreads)
     // behind), and they only choose which of this CTA's first tiles to prefetch
     // into L2 (a prefetch reads no value; L2 is where writes land, so a line
     // prefetched early is never stale).  Everything is read again after the
-    // wait.  This fills the DRAM idle time at the previous kernel's tail.
-    if constexpr (MODE == kModePaged) {
-        if (p.prefetch_tiles > 0) {
-            const int ss = p.lpt ? longest_first(true) : s;
+    // wait.  This fills the DRAM idle time at the previous kernel's tail.  The
+    // tiled step's tile counts and tile lists are treated the same way.
+    if (p.prefetch_tiles > 0) {
+        int t0 = 0, t1 = 0, ss = s;
+        const int32_t *ids;
+        if constexpr (MODE == kModePaged) {
+            ss = p.lpt ? longest_first(true) : s;
             int L = __ldcg(p.context_lens + ss);
             L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
             const int chunk = split_chunk_tokens(L, p.num_splits, bs, p.min_kv_per_split);
             const long long a = static_cast<long long>(split) * chunk;
-            const int t0 = static_cast<int>(a < L ? a : L);
-            const int t1 = static_cast<int>(a + chunk < L ? a + chunk : L);
-            if (t0 < t1) {
-                const int tile0 = t0 / kTileTokens;
-                const int ntiles = (t1 + kTileTokens - 1) / kTileTokens - tile0;
-                const int V = max(1, min(p.max_parts, (ntiles + p.part_tiles - 1) / p.part_tiles));
-                const int j = C == 1 ? 0 : part;
-                if (j < V) {
-                    const int my0 = tile0 + (j * ntiles) / V;
-                    const int n = min(tile0 + ((j + 1) * ntiles) / V - my0, p.prefetch_tiles);
-                    const int32_t *ids = p.block_table + static_cast<long long>(ss) * p.max_blocks_per_seq;
-                    for (int t = tid; t < n; t += kThreads) {
-                        const int gt = my0 + t;
-                        const int id = __ldcg(ids + gt / tiles_per_block);
-                        if (id >= 0 && id < p.num_blocks) {
-                            const int sub = (gt % tiles_per_block) * kTileTokens;
-                            const int c1 = p.tok_dim == 1 ? sub : kvh;
-                            const int c2 = p.tok_dim == 1 ? kvh : sub;
+            t0 = static_cast<int>(a < L ? a : L);
+            t1 = static_cast<int>(a + chunk < L ? a + chunk : L);
+            ids = p.block_table + static_cast<long long>(ss) * p.max_blocks_per_seq;
+        } else {
+            int cnt = __ldcg(p.tile_counts + s);
+            cnt = cnt < 0 ? 0 : (cnt > p.tile_capacity ? p.tile_capacity : cnt);
+            const int lv = (p.last_valid >= 1 && p.last_valid < bs) ? p.last_valid : bs;
+            t1 = cnt > 0 ? (cnt - 1) * bs + lv : 0;
+            ids = p.tile_blocks + static_cast<long long>(s) * p.tile_capacity;
+        }
+        if (t0 < t1) {
+            const int tile0 = t0 / kTileTokens;
+            const int ntiles = (t1 + kTileTokens - 1) / kTileTokens - tile0;
+            const int V = max(1, min(p.max_parts, (ntiles + p.part_tiles - 1) / p.part_tiles));
+            const int j = C == 1 ? 0 : part;
+            if (j < V) {
+                const int my0 = tile0 + (j * ntiles) / V;
+                const int n = min(tile0 + ((j + 1) * ntiles) / V - my0, p.prefetch_tiles);
+                for (int t = tid; t < n; t += kThreads) {
+                    const int gt = my0 + t;
+                    const int id = __ldcg(ids + gt / tiles_per_block);
+                    if (id >= 0 && id < p.num_blocks) {
+                        const int sub = (gt % tiles_per_block) * kTileTokens;
+                        const int c1 = p.tok_dim == 1 ? sub : kvh;
+                        const int c2 = p.tok_dim == 1 ? kvh : sub;
 #pragma unroll
-                            for (int b = 0; b < NBOX; ++b) {
-                                dev::tma_prefetch_4d(&tmk, b * kBoxCols, c1, c2, id);
-                                dev::tma_prefetch_4d(&tmv, b * kBoxCols, c1, c2, id);
-                            }
+                        for (int b = 0; b < NBOX; ++b) {
+                            dev::tma_prefetch_4d(&tmk, b * kBoxCols, c1, c2, id);
+                            dev::tma_prefetch_4d(&tmv, b * kBoxCols, c1, c2, id);
                         }
                     }
                 }

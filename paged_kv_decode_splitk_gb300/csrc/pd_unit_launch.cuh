@@ -12,39 +12,45 @@ int unit_smem_bytes(int dpad, int rows, int stages);
 
 template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
 cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p_in,
-                        long long units, int smem_bytes, cudaStream_t stream, int layout) {
+                        long long units, int stages_seq, cudaStream_t stream, int layout) {
     auto kern = unit_kernel<DPAD, GN, HL, MODE, PACKED>;
-    // Raise the kernel's dynamic shared-memory limit once per device (and
-    // again only if a launch asks for more); remember the SM count and how
-    // many CTAs of this kernel fit on one SM at that size.
+    // Per device: the dynamic shared-memory limit raised so far, the SM count,
+    // and how many CTAs of this kernel fit on one SM at each stage count.
     static std::mutex mu;
     static int configured[64] = {0};
-    static int per_sm[64] = {0};
     static int sm_count[64] = {0};
+    static int per_sm[64][kMaxStagesPerWarp + 1] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int slots = 0;
-    {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (p_in.stages < 1 || p_in.stages > kMaxStagesPerWarp || stages_seq < 1 || stages_seq > kMaxStagesPerWarp)
+        return cudaErrorInvalidValue;
+    auto slots_for = [&](int stages, int *smem_out) -> cudaError_t {
+        const int smem = unit_smem_plan(DPAD, 8 * GN, stages).total;
+        *smem_out = smem;
         std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (configured[dev] != smem_bytes) {
-            if (configured[dev] < smem_bytes) {
-                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-                if (e != cudaSuccess) return e;
-            }
-            int n = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem_bytes);
-            if (e != cudaSuccess) return e;
-            if (!sm_count[dev]) {
-                e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-                if (e != cudaSuccess) return e;
-            }
-            per_sm[dev] = n;
-            if (configured[dev] < smem_bytes) configured[dev] = smem_bytes;
+        if (configured[dev] < smem) {
+            cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e2 != cudaSuccess) return e2;
+            configured[dev] = smem;
         }
-        slots = per_sm[dev] * sm_count[dev];
-    }
+        if (!sm_count[dev]) {
+            cudaError_t e2 = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+            if (e2 != cudaSuccess) return e2;
+        }
+        if (!per_sm[dev][stages]) {
+            int n = 0;
+            cudaError_t e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
+            if (e2 != cudaSuccess) return e2;
+            per_sm[dev][stages] = n > 0 ? n : -1;
+        }
+        return cudaSuccess;
+    };
+    int smem_bytes = 0;
+    e = slots_for(p_in.stages, &smem_bytes);
+    if (e != cudaSuccess) return e;
+    const int slots = per_sm[dev][p_in.stages] > 0 ? per_sm[dev][p_in.stages] * sm_count[dev] : 0;
     // Where the parts of a unit run.  Both layouts fold the same parts in the
     // same order, so the choice changes timing only, never the output bits:
     // when one CTA per part still fits in about one wave, a cluster of
@@ -61,10 +67,18 @@ cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const Un
     p.cluster = C;
     const long long grid_x = units * C;
     if (grid_x > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    // A grid of many short units (several waves, one CTA per unit) keeps more
+    // loads in flight with a deeper ring per warp; a single-wave grid keeps
+    // the shallower one and more CTAs per SM.  Stages change no result.
+    if (C == 1 && stages_seq != p.stages && grid_x > slots) {
+        e = slots_for(stages_seq, &smem_bytes);
+        if (e != cudaSuccess) return e;
+        p.stages = stages_seq;
+    }
     // The early L2 prefetch pays off only for CTAs that are resident while the
-    // previous kernel drains, i.e. a grid that fits in one wave; CTAs of later
+    // previous kernel drains, i.e. a grid of about one wave; CTAs of later
     // waves would just read the lengths and the block table twice.
-    if (grid_x > slots) p.prefetch_tiles = 0;
+    if (grid_x * 4 > static_cast<long long>(slots) * 5) p.prefetch_tiles = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_x));
     cfg.blockDim = dim3(kThreads);

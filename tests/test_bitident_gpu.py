@@ -157,3 +157,20 @@ def test_part_layout_does_not_change_bits(cuda_device, kind):
     finally:
         pd.pd_debug_set_tuning(0, 0, -1)
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_ring_depth_does_not_change_bits(cuda_device):
+    """The ring depth per warp is a launch choice (a launch of several waves of
+    one-CTA units takes a deeper ring than a single-wave one): the per-warp
+    tile order and every fold are the same, so no bit may change."""
+    lens = [int(x) for x in np.random.default_rng(5).integers(200, 2000, size=160)]
+    w = W.custom(lens, 32, 8, 128, seed=75)   # 160 x 8 x 10 units: several waves
+    outs = []
+    try:
+        for tun in ((0, 0, -1), (1, 1, -1), (2, 1, -1), (3, 1, -1)):
+            pd.pd_debug_set_tuning(*tun)
+            outs.append(_bits(w, cuda_device, 10))
+    finally:
+        pd.pd_debug_set_tuning(0, 0, -1)
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
