@@ -5,7 +5,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--w
 A step is one pass of the whole decode path over one batch of synthetic input
 (for the paged workloads: one pd_decode_attn call, i.e. the unit pass plus the
 merge when the launch splits; for the tiled workload: begin, every step_tile
-call and finalize).  The default workload is the GQA-packed one: 32 sequences
+call and finalize; for the mixed tiled workload: one pd_tiled_run, i.e. begin,
+the step_tile calls over the paged cache and then the scratch pool, finalize).  The default workload is the GQA-packed one: 32 sequences
 with lengths uniform in [512, 4096], 16 query heads over 2 KV heads, head dim
 256, block 16, non-split launch through the packed pass.
 
@@ -148,7 +149,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
 
     w = _workload(args.workload)
-    tiled = args.workload == "tiled"
+    mixed = args.workload == "tiled_mixed"
+    tiled = args.workload == "tiled" or mixed
     kv_bytes = w.kv_bytes
     stream = torch.cuda.current_stream()
 
@@ -167,6 +169,35 @@ def run_ours(args):
             api.decode_attn(base.q, ks[i % copies], vs[i % copies], base.block_table, base.context_lens,
                             w.inv_sqrt_d, n, w.gqa_pack, out, wsp)
         l2_note = f"rotating {copies} KV-cache copies ({copies * pool_bytes / 1e6:.0f} MB > 129 MB L2)"
+    elif mixed:
+        # one pd_tiled_run per step: begin, the paged-cache calls, the scratch-pool
+        # calls, finalize
+        base = api.MixedTiledInputs(w, dev)
+        n = 1
+        pool_bytes = (base.paged_k.numel() + base.paged_v.numel() + base.scratch.numel()) * 2
+        copies = max(2, -(-3 * L2_BYTES // pool_bytes))
+        t = pd.Tiled(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.tile_capacity)
+        stripe = w.num_kv_heads * w.block_size * w.head_dim
+        srcs = []
+        for i in range(copies):
+            pk = base.paged_k if i == 0 else base.paged_k.clone()
+            pv = base.paged_v if i == 0 else base.paged_v.clone()
+            sc = (base.scratch if i == 0 else base.scratch.clone()).view(-1)
+            lst = []
+            for ci, (kind, _, _, lb) in enumerate(w.calls):
+                if kind == "paged":
+                    lst.append((pk, pv, base.tile_blocks[ci], base.tile_counts[ci], t.paged_strides(), lb))
+                else:
+                    lst.append((sc, sc[stripe:], base.tile_blocks[ci], base.tile_counts[ci],
+                                t.scratch_pool_strides(), lb))
+            srcs.append(lst)
+        out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
+        launches_per_step = 2 + len(w.calls)
+
+        def step(i):
+            t.run(base.q, srcs[i % copies], out, w.num_seqs)
+        l2_note = (f"rotating {copies} copies of the paged cache and scratch pool "
+                   f"({copies * pool_bytes / 1e6:.0f} MB > 129 MB L2)")
     else:
         base = api.TiledInputs(w, dev)
         n = 1
@@ -337,7 +368,7 @@ def run_ours(args):
                 "head_dim": w.head_dim,
                 "block_size": w.block_size,
                 "num_splits": n,
-                "gqa_pack": bool(w.__dict__.get("gqa_pack", False)),
+                "gqa_pack": int(w.__dict__.get("gqa_pack", 0)),
                 "kv_bytes_per_step": kv_bytes,
                 "tokens": int(w.context_lens.sum()) if not tiled else w.kv_tokens,
                 "l2": l2_note,
@@ -373,6 +404,17 @@ def _oracle_step(w, seqs):
         return oracle.decode_attn(w.q[seqs], w.k_cache, w.v_cache, w.block_table[seqs],
                                   w.context_lens[seqs], w.inv_sqrt_d)
     from paged_kv_decode_splitk_gb300 import workloads as W
+    if hasattr(w, "calls"):
+        kf, vf = W.scratch_pool_views(w.scratch)
+        Hkv, D, bs = w.num_kv_heads, w.head_dim, w.block_size
+        calls = []
+        for kind, tb, tc, lb in w.calls:
+            paged = kind == "paged"
+            calls.append(dict(k_pool=w.paged_k if paged else kf, v_pool=w.paged_v if paged else vf,
+                              tile_blocks=tb[seqs], tile_block_counts=tc[seqs], last_block_valid_slots=lb,
+                              strides=(oracle.paged_strides if paged else oracle.scratch_pool_strides)(
+                                  Hkv, D, bs)))
+        return oracle.tiled_attn_multi(w.q[seqs], calls, Hkv, bs)
     kf, vf = W.scratch_pool_views(w.pool)
     return oracle.tiled_attn(w.q[seqs], kf, vf, w.tile_blocks[:, seqs], w.tile_block_counts[:, seqs],
                              w.last_block_valid_slots, w.num_kv_heads, w.block_size,
@@ -384,6 +426,13 @@ def _seq_bytes(w, seqs):
         return int(w.context_lens[seqs].astype("int64").sum()) * w.num_kv_heads * w.head_dim * 4
     bs = w.block_size
     tok = 0
+    if hasattr(w, "calls"):
+        for _, _, tc, lb in w.calls:
+            for s in seqs:
+                cnt = int(tc[s])
+                if cnt:
+                    tok += (cnt - 1) * bs + (lb if 1 <= lb < bs else bs)
+        return tok * w.num_kv_heads * w.head_dim * 4
     for c in range(w.num_calls):
         lb = int(w.last_block_valid_slots[c])
         for s in seqs:
@@ -470,7 +519,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_packed",
-                    choices=["tiny", "gqa_packed", "long_context", "large_batch", "tiled"])
+                    choices=["tiny", "gqa_packed", "gqa_packed_splitk", "long_context", "large_batch", "tiled",
+                             "tiled_mixed"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

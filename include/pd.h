@@ -62,6 +62,11 @@ extern "C" {
 #define PD_SPLITK_TARGET_WAVES 2
 #define PD_GQA_PACK_WIDTH 8
 #define PD_GQA_PACK_HEAD_DIM 256
+
+/* Values of pd_decode_attn's gqa_pack argument. */
+#define PD_GQA_PACK_OFF 0
+#define PD_GQA_PACK_ON 1
+#define PD_GQA_PACK_SPLITK 2
 #define PD_MIN_KV_PER_SPLIT 256
 #define PD_MAX_HEAD_DIM 256
 
@@ -181,9 +186,15 @@ int pd_split_chunk_tokens(int context_len, int num_splits, int block_size);
  *                head_dim, num_splits) bytes, 16-B aligned; may be NULL when
  *                num_splits == 1.  Contents on entry are ignored; on return they
  *                are scratch.
- *   gqa_pack     0: split-K path.  1: the GQA-packed pass; it applies only when
- *                num_splits == 1 and pd_gqa_pack_shape_ok(), otherwise the call
- *                returns PD_NOT_APPLICABLE and launches nothing.
+ *   gqa_pack     PD_GQA_PACK_OFF (0): split-K path.  PD_GQA_PACK_ON (1): the
+ *                GQA-packed pass; it applies only when num_splits == 1 and
+ *                pd_gqa_pack_shape_ok(), otherwise the call returns
+ *                PD_NOT_APPLICABLE and launches nothing.  PD_GQA_PACK_SPLITK (2):
+ *                the packed pass with any split count (no counterpart on the
+ *                pages, which gate packing to non-split launches): same shape
+ *                gate, and with num_splits > 1 each (sequence, KV head, split)
+ *                writes its partial to the workspace and the merge pass folds
+ *                them, exactly as on the split-K path.
  * Shape limits: num_q_heads a positive multiple of num_kv_heads; head_dim a
  * multiple of 8 in [8, 256]; block_size a multiple of 16 in [16, 256].
  * Every path serves a whole group of query heads from one read of K and V,
@@ -307,6 +318,32 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
 /* TiledAttention::finalize: out [num_seqs, Hq, head_dim] BF16 = o / l, and 0
  * where l is 0.  Returns PD_OK, PD_ERR_CAPACITY, PD_ERR_INVALID or PD_ERR_CUDA. */
 int pd_tiled_finalize(pd_tiled *t, void *out, int num_seqs, void *stream);
+
+/* One step_tile call of a multi-call step: the pools, tile list and strides
+ * that call reads (tiled_attention.rs page: step_tile takes them per call, so
+ * one step may mix sources, e.g. resident blocks in the paged cache and
+ * swapped-in blocks in the scratch pool).  Fields as for pd_tiled_step. */
+typedef struct pd_tiled_source {
+    const void *k_pool;
+    const void *v_pool;
+    const int32_t *tile_blocks;        /* [num_seqs, tile_capacity] int32 */
+    const int32_t *tile_block_counts;  /* [num_seqs] int32 */
+    int64_t blk_stride;
+    int64_t tok_stride;
+    int64_t kvh_stride;
+    int last_block_valid_slots;
+} pd_tiled_source;
+
+/* A whole tiled decode step in one call: begin_step, one step_tile per source
+ * in array order, finalize into out [num_seqs, Hq, head_dim] BF16 (the
+ * tiled_attention.rs page's per-step sequence, driven from one place).  Every
+ * source is checked before anything launches, so an invalid argument leaves
+ * the running state and `out` untouched.  The result equals one begin, the
+ * steps and one finalize made separately (same kernels, same order).
+ * num_sources may be 0 (out = 0).  Returns PD_OK, PD_ERR_CAPACITY,
+ * PD_ERR_INVALID or PD_ERR_CUDA. */
+int pd_tiled_run(pd_tiled *t, const void *q, const pd_tiled_source *sources, int num_sources,
+                 void *out, int num_seqs, void *stream);
 
 /* ---- diagnostics ---- */
 

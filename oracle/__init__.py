@@ -62,7 +62,10 @@ def _load():
                                              ctypes.c_float, p]
             lib.orc_tiled_attn.argtypes = [p, p, p, i64, p, p, p, i32, i32, i32, i32, i32, i32,
                                            i32, i64, i64, i64, p]
-            for f in (lib.orc_decode_attn, lib.orc_split_replay, lib.orc_tiled_attn):
+            lib.orc_tiled_attn_multi.argtypes = [p, p, p, p, p, p, p, p, p, i32, i32, i32, i32,
+                                                 i32, i32, p]
+            for f in (lib.orc_decode_attn, lib.orc_split_replay, lib.orc_tiled_attn,
+                      lib.orc_tiled_attn_multi):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -145,6 +148,42 @@ def tiled_attn(q, k_pool, v_pool, tile_blocks, tile_block_counts, last_block_val
                                 _ptr(tc), _ptr(lb), T, S, Hq, num_kv_heads, D, block_size, tcap,
                                 blk, tok, kvh, _ptr(out))
     _check(rc, "tiled_attn")
+    return out
+
+
+def tiled_attn_multi(q, calls, num_kv_heads: int, block_size: int) -> np.ndarray:
+    """Result of begin_step, one step_tile per call and finalize, FP64, where each
+    call names its own source (tiled_attention.rs page: step_tile takes the pools
+    and the strides per call).
+
+    calls: sequence of dicts with k_pool, v_pool (flat uint16 arrays the strides
+    address), tile_blocks [S, tcap] int32, tile_block_counts [S] int32,
+    last_block_valid_slots (int) and strides (blk, tok, kvh).
+    """
+    q = _u16(q)
+    S, Hq, D = q.shape
+    T = len(calls)
+    kp = [_u16(np.asarray(c["k_pool"]).reshape(-1)) for c in calls]
+    vp = [_u16(np.asarray(c["v_pool"]).reshape(-1)) for c in calls]
+    tb = [_i32(c["tile_blocks"]) for c in calls]
+    tc = [_i32(c["tile_block_counts"]) for c in calls]
+    for c in range(T):
+        assert tb[c].ndim == 2 and tb[c].shape[0] == S and tc[c].shape == (S,)
+    P = ctypes.c_void_p
+    k_arr = (P * max(1, T))(*[_ptr(a) for a in kp])
+    v_arr = (P * max(1, T))(*[_ptr(a) for a in vp])
+    tb_arr = (P * max(1, T))(*[_ptr(a) for a in tb])
+    tc_arr = (P * max(1, T))(*[_ptr(a) for a in tc])
+    elems = np.array([min(kp[c].size, vp[c].size) for c in range(T)] or [0], dtype=np.int64)
+    strides = np.array([int(x) for c in calls for x in c["strides"]] or [0, 0, 0], dtype=np.int64)
+    tcap = np.array([tb[c].shape[1] for c in range(T)] or [0], dtype=np.int32)
+    lb = np.array([int(c["last_block_valid_slots"]) for c in calls] or [0], dtype=np.int32)
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    rc = _load().orc_tiled_attn_multi(_ptr(q), ctypes.cast(k_arr, P), ctypes.cast(v_arr, P),
+                                      _ptr(elems), _ptr(strides), ctypes.cast(tb_arr, P),
+                                      ctypes.cast(tc_arr, P), _ptr(tcap), _ptr(lb), T, S, Hq,
+                                      num_kv_heads, D, block_size, _ptr(out))
+    _check(rc, "tiled_attn_multi")
     return out
 
 

@@ -39,6 +39,9 @@
  *   1 .. block_size-1 mean a full block), K and V addressed through the
  *   (blk, tok, kvh) element strides the caller passes, and the scale
  *   1/sqrt(head_dim) rounded to FP32 because step_tile carries no scale.
+ *   orc_tiled_attn_multi is the same with every call naming its own K and V
+ *   pools and strides (the page's step_tile takes them per call, so one step
+ *   may mix the paged layout and the scratch-pool layout).
  *
  * Return codes: 0 ok, -1 bad argument, -2 out of memory, -3 a block id or
  * context length outside the buffers the caller described.
@@ -345,6 +348,87 @@ int orc_tiled_attn(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_
                         }
                         krows[n] = k_pool + off;
                         vrows[n] = v_pool + off;
+                        ++n;
+                    }
+                    if (rc != 0)
+                        break;
+                }
+            }
+            if (rc != 0)
+                break;
+            const uint16_t *qrow = q + ((int64_t)s * num_q_heads + h) * head_dim;
+            double *o = out + ((int64_t)s * num_q_heads + h) * head_dim;
+            attend_direct(qrow, krows, vrows, n, head_dim, scale, x, o);
+        }
+    }
+done:
+    free(krows);
+    free(vrows);
+    free(x);
+    return rc;
+}
+
+/*
+ * The tiled step over calls that each name their own source: call c reads K
+ * from k_pools[c] and V from v_pools[c] (both bounded by pool_elems[c]
+ * elements) at blk*strides[3c] + tok*strides[3c+1] + kvh*strides[3c+2], with
+ * tile_blocks[c] [num_seqs, tile_capacity[c]], tile_block_counts[c]
+ * [num_seqs] and last_block_valid_slots[c].  The token set and the scale are
+ * those of orc_tiled_attn.
+ */
+int orc_tiled_attn_multi(const uint16_t *q, const uint16_t *const *k_pools,
+                         const uint16_t *const *v_pools, const int64_t *pool_elems,
+                         const int64_t *strides, const int32_t *const *tile_blocks,
+                         const int32_t *const *tile_block_counts, const int32_t *tile_capacity,
+                         const int32_t *last_block_valid_slots, int num_calls, int num_seqs,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         double *out)
+{
+    if (check_heads(num_q_heads, num_kv_heads, head_dim, block_size) != 0 || num_seqs < 0 ||
+        num_calls < 0)
+        return -1;
+    int64_t max_tok = 0;
+    for (int c = 0; c < num_calls; ++c) {
+        if (tile_capacity[c] < 0)
+            return -1;
+        max_tok += (int64_t)tile_capacity[c] * block_size;
+    }
+    const uint16_t **krows = malloc(sizeof(*krows) * (size_t)(max_tok + 1));
+    const uint16_t **vrows = malloc(sizeof(*vrows) * (size_t)(max_tok + 1));
+    double *x = malloc(sizeof(double) * (size_t)(max_tok + 1));
+    int rc = 0;
+    if (!krows || !vrows || !x) {
+        rc = -2;
+        goto done;
+    }
+    int G = num_q_heads / num_kv_heads;
+    double scale = (double)(float)(1.0 / sqrt((double)head_dim));
+    for (int s = 0; s < num_seqs && rc == 0; ++s) {
+        for (int h = 0; h < num_q_heads && rc == 0; ++h) {
+            int kvh = h / G;
+            int64_t n = 0;
+            for (int c = 0; c < num_calls && rc == 0; ++c) {
+                int tcap = tile_capacity[c];
+                int cnt = tile_block_counts[c][s];
+                if (cnt < 0 || cnt > tcap) {
+                    rc = -3;
+                    break;
+                }
+                int lb = last_block_valid_slots[c];
+                for (int i = 0; i < cnt; ++i) {
+                    int64_t blk = tile_blocks[c][(int64_t)s * tcap + i];
+                    int ntok = block_size;
+                    if (i == cnt - 1 && lb >= 1 && lb < block_size)
+                        ntok = lb;
+                    for (int t = 0; t < ntok; ++t) {
+                        int64_t off = blk * strides[3 * c] + (int64_t)t * strides[3 * c + 1] +
+                                      (int64_t)kvh * strides[3 * c + 2];
+                        if (blk < 0 || off < 0 || off + head_dim > pool_elems[c]) {
+                            rc = -3;
+                            break;
+                        }
+                        krows[n] = k_pools[c] + off;
+                        vrows[n] = v_pools[c] + off;
                         ++n;
                     }
                     if (rc != 0)

@@ -126,3 +126,50 @@ def run_tiled(inp: TiledInputs, tiled: pd.Tiled | None = None, out=None, stream=
             torch.cuda.current_stream().synchronize()
             tiled.close()
     return out
+
+
+class MixedTiledInputs:
+    """Device copies of a workloads.MixedTiledWorkload."""
+
+    def __init__(self, mw, device="cuda"):
+        self.w = mw
+        self.device = torch.device(device)
+        self.q = bf16_tensor(mw.q, self.device)
+        self.paged_k = bf16_tensor(mw.paged_k, self.device)
+        self.paged_v = bf16_tensor(mw.paged_v, self.device)
+        self.scratch = bf16_tensor(mw.scratch, self.device)
+        flat = self.scratch.view(-1)
+        stripe = mw.num_kv_heads * mw.block_size * mw.head_dim
+        self.scratch_k = flat
+        self.scratch_v = flat[stripe:]
+        self.tile_blocks = [i32_tensor(c[1], self.device) for c in mw.calls]
+        self.tile_counts = [i32_tensor(c[2], self.device) for c in mw.calls]
+
+    def sources(self, tiled: pd.Tiled):
+        out = []
+        for i, (kind, _, _, lbvs) in enumerate(self.w.calls):
+            if kind == "paged":
+                k, v, st = self.paged_k, self.paged_v, tiled.paged_strides()
+            else:
+                k, v, st = self.scratch_k, self.scratch_v, tiled.scratch_pool_strides()
+            out.append((k, v, self.tile_blocks[i], self.tile_counts[i], st, int(lbvs)))
+        return out
+
+
+def run_tiled_mixed(inp: MixedTiledInputs, tiled: pd.Tiled | None = None, out=None, stream=None):
+    """One pd_tiled_run: begin, one step per source (paged, then scratch pool), finalize."""
+    mw = inp.w
+    own = tiled is None
+    if own:
+        tiled = pd.Tiled(mw.num_seqs, mw.num_q_heads, mw.num_kv_heads, mw.head_dim, mw.block_size,
+                         mw.tile_capacity)
+    try:
+        if out is None:
+            out = torch.empty((mw.num_seqs, mw.num_q_heads, mw.head_dim), dtype=torch.bfloat16,
+                              device=inp.device)
+        tiled.run(inp.q, inp.sources(tiled), out, mw.num_seqs, stream)
+    finally:
+        if own:
+            torch.cuda.current_stream().synchronize()
+            tiled.close()
+    return out

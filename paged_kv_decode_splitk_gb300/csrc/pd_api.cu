@@ -475,9 +475,10 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
                    float inv_sqrt_d, int num_splits, void *workspace, size_t workspace_bytes,
                    int gqa_pack, void *stream) {
-    if (gqa_pack != 0 && gqa_pack != 1) return fail(PD_ERR_INVALID, "gqa_pack must be 0 or 1");
+    if (gqa_pack < PD_GQA_PACK_OFF || gqa_pack > PD_GQA_PACK_SPLITK)
+        return fail(PD_ERR_INVALID, "gqa_pack must be 0, 1 or 2");
     if (gqa_pack) {
-        if (num_splits != 1)
+        if (gqa_pack == PD_GQA_PACK_ON && num_splits != 1)
             return fail(PD_NOT_APPLICABLE, "GQA-packed pass serves non-split launches only (num_splits=%d)",
                         num_splits);
         if (!pd_gqa_pack_shape_ok(num_q_heads, num_kv_heads, head_dim))
@@ -511,7 +512,7 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     }
 
     const int G = num_q_heads / num_kv_heads;
-    const bool packed = gqa_pack == 1;
+    const bool packed = gqa_pack != PD_GQA_PACK_OFF;
     const int dpad = packed ? PD_GQA_PACK_HEAD_DIM : dpad_for(head_dim);
     const int gn = packed ? 1 : (G <= 8 ? 1 : 2);
     const int rows = 8 * gn;
@@ -718,15 +719,18 @@ int pd_tiled_begin(pd_tiled *t, int num_seqs, void *stream) {
 // PD_DEV_BAD_BLOCK_ID).
 constexpr long long kTiledBlockExtent = 1LL << 24;
 
-int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_pool,
-                  const int32_t *tile_blocks, const int32_t *tile_block_counts, int num_seqs,
-                  int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
-                  int last_block_valid_slots, void *stream) {
+namespace {
+// Argument checks of one step_tile call.  PD_OK with *skip set when the call
+// has nothing to fold (no sequence, or a zero tile capacity).
+int check_step(const pd_tiled *t, const void *q, const void *k_pool, const void *v_pool,
+               const int32_t *tile_blocks, const int32_t *tile_block_counts, int num_seqs,
+               int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride, bool *skip) {
+    *skip = true;
     if (!t) return fail(PD_ERR_INVALID, "null handle");
     if (num_seqs < 0) return fail(PD_ERR_INVALID, "num_seqs %d < 0", num_seqs);
     if (num_seqs > t->dims.max_seqs)
         return fail(PD_ERR_CAPACITY, "step_tile num_seqs %d > max_seqs %d", num_seqs, t->dims.max_seqs);
-    if (num_seqs == 0 || t->dims.tile_capacity == 0) return ok();
+    if (num_seqs == 0 || t->dims.tile_capacity == 0) return PD_OK;
     if (!q || !k_pool || !v_pool || !tile_blocks || !tile_block_counts)
         return fail(PD_ERR_INVALID, "null pointer");
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
@@ -737,6 +741,20 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
                     "strides (blk %lld, tok %lld, kvh %lld) must be positive multiples of 8 elements",
                     static_cast<long long>(blk_stride), static_cast<long long>(tok_stride),
                     static_cast<long long>(kvh_stride));
+    *skip = false;
+    return PD_OK;
+}
+}  // namespace
+
+int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_pool,
+                  const int32_t *tile_blocks, const int32_t *tile_block_counts, int num_seqs,
+                  int64_t blk_stride, int64_t tok_stride, int64_t kvh_stride,
+                  int last_block_valid_slots, void *stream) {
+    bool skip = true;
+    const int crc = check_step(t, q, k_pool, v_pool, tile_blocks, tile_block_counts, num_seqs,
+                               blk_stride, tok_stride, kvh_stride, &skip);
+    if (crc != PD_OK) return crc;
+    if (skip) return ok();
     const pd_tiled_dims &d = t->dims;
     const int G = d.num_q_heads / d.num_kv_heads;
     const int dpad = dpad_for(d.head_dim);
@@ -813,6 +831,38 @@ int pd_tiled_finalize(pd_tiled *t, void *out, int num_seqs, void *stream) {
                                               static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tiled finalize launch");
     return ok();
+}
+
+int pd_tiled_run(pd_tiled *t, const void *q, const pd_tiled_source *sources, int num_sources,
+                 void *out, int num_seqs, void *stream) {
+    if (!t) return fail(PD_ERR_INVALID, "null handle");
+    if (num_sources < 0) return fail(PD_ERR_INVALID, "num_sources %d < 0", num_sources);
+    if (num_sources > 0 && !sources) return fail(PD_ERR_INVALID, "null sources");
+    if (num_seqs < 0) return fail(PD_ERR_INVALID, "num_seqs %d < 0", num_seqs);
+    if (num_seqs > t->dims.max_seqs)
+        return fail(PD_ERR_CAPACITY, "num_seqs %d > max_seqs %d", num_seqs, t->dims.max_seqs);
+    if (num_seqs > 0 && !out) return fail(PD_ERR_INVALID, "null out");
+    for (int i = 0; i < num_sources; ++i) {
+        const pd_tiled_source &src = sources[i];
+        bool skip = true;
+        const int crc = check_step(t, q, src.k_pool, src.v_pool, src.tile_blocks, src.tile_block_counts,
+                                   num_seqs, src.blk_stride, src.tok_stride, src.kvh_stride, &skip);
+        if (crc != PD_OK) {
+            char msg[512];
+            snprintf(msg, sizeof msg, "source %d: %s", i, pd_last_error());
+            return fail(crc, "%s", msg);
+        }
+    }
+    int rc = pd_tiled_begin(t, num_seqs, stream);
+    if (rc != PD_OK) return rc;
+    for (int i = 0; i < num_sources; ++i) {
+        const pd_tiled_source &src = sources[i];
+        rc = pd_tiled_step(t, q, src.k_pool, src.v_pool, src.tile_blocks, src.tile_block_counts, num_seqs,
+                           src.blk_stride, src.tok_stride, src.kvh_stride, src.last_block_valid_slots,
+                           stream);
+        if (rc != PD_OK) return rc;
+    }
+    return pd_tiled_finalize(t, out, num_seqs, stream);
 }
 
 // ---- diagnostics ------------------------------------------------------------------------------

@@ -30,6 +30,10 @@ PD_ERR_CUDA = -4
 PD_ERR_ALLOC = -5
 PD_ERR_UNSUPPORTED = -6
 
+PD_GQA_PACK_OFF = 0
+PD_GQA_PACK_ON = 1
+PD_GQA_PACK_SPLITK = 2
+
 PD_POLICY_LEGACY = 0
 PD_POLICY_AUTO = 1
 PD_POLICY_PINNED = 2
@@ -56,6 +60,13 @@ class pd_tiled_dims(ctypes.Structure):
     _fields_ = [("max_seqs", ctypes.c_int), ("num_q_heads", ctypes.c_int),
                 ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("block_size", ctypes.c_int), ("tile_capacity", ctypes.c_int)]
+
+
+class pd_tiled_source(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("tile_blocks", ctypes.c_void_p), ("tile_block_counts", ctypes.c_void_p),
+                ("blk_stride", ctypes.c_int64), ("tok_stride", ctypes.c_int64),
+                ("kvh_stride", ctypes.c_int64), ("last_block_valid_slots", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -96,6 +107,7 @@ _SIGS = {
     "pd_tiled_begin": (_I, [_VP, _I, _VP]),
     "pd_tiled_step": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I64, _I64, _I64, _I, _VP]),
     "pd_tiled_finalize": (_I, [_VP, _VP, _I, _VP]),
+    "pd_tiled_run": (_I, [_VP, _VP, _VP, _I, _VP, _I, _VP]),
     "pd_device_status": (_I, [_VP]),
     "pd_debug_fail_next_allocs": (None, [_I]),
     "pd_debug_set_tuning": (None, [_I, _I, _I]),
@@ -230,7 +242,7 @@ def pd_split_chunk_tokens(context_len: int, num_splits: int, block_size: int) ->
 # ---- paged decode -----------------------------------------------------------------
 
 def pd_decode_attn(q, k_cache, v_cache, block_table, context_lens, out, inv_sqrt_d: float,
-                   num_splits: int, workspace=None, gqa_pack: bool = False, stream=None,
+                   num_splits: int, workspace=None, gqa_pack: int = 0, stream=None,
                    num_blocks: int | None = None) -> int:
     """out[S, Hq, D] <- paged-decode attention (see pd.h).  Shapes come from the tensors:
     q [S, Hq, D]; k_cache / v_cache [num_blocks, block_size, Hkv, D] BF16; block_table
@@ -242,7 +254,7 @@ def pd_decode_attn(q, k_cache, v_cache, block_table, context_lens, out, inv_sqrt
     rc = lib().pd_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                               int(block_table.shape[1]), _ptr(context_lens), _ptr(out), S, Hq, Hkv,
                               D, bs, nb if num_blocks is None else num_blocks, float(inv_sqrt_d),
-                              int(num_splits), _ptr(workspace), ws_bytes, int(bool(gqa_pack)),
+                              int(num_splits), _ptr(workspace), ws_bytes, int(gqa_pack),
                               _stream(stream))
     return _check(rc)
 
@@ -311,6 +323,9 @@ class Tiled:
     def finalize(self, out, num_seqs, stream=None):
         return pd_tiled_finalize(self.handle, out, num_seqs, stream)
 
+    def run(self, q, sources, out, num_seqs, stream=None):
+        return pd_tiled_run(self.handle, q, sources, out, num_seqs, stream)
+
     def state(self):
         return pd_tiled_state(self.handle)
 
@@ -359,6 +374,17 @@ def pd_tiled_step(handle: int, q, k_pool, v_pool, tile_blocks, tile_block_counts
     return _check(lib().pd_tiled_step(handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(tile_blocks),
                                       _ptr(tile_block_counts), num_seqs, blk, tok, kvh,
                                       int(last_block_valid_slots), _stream(stream)))
+
+
+def pd_tiled_run(handle: int, q, sources, out, num_seqs: int, stream=None) -> int:
+    """begin, one step per source, finalize.  sources: sequence of
+    (k_pool, v_pool, tile_blocks, tile_block_counts, strides, last_block_valid_slots)."""
+    arr = (pd_tiled_source * max(1, len(sources)))()
+    for i, (k, v, tb, tc, strides, lbvs) in enumerate(sources):
+        blk, tok, kvh = (int(x) for x in strides)
+        arr[i] = pd_tiled_source(_ptr(k), _ptr(v), _ptr(tb), _ptr(tc), blk, tok, kvh, int(lbvs))
+    return _check(lib().pd_tiled_run(handle, _ptr(q), ctypes.cast(arr, _VP) if sources else None,
+                                     len(sources), _ptr(out), num_seqs, _stream(stream)))
 
 
 def pd_tiled_finalize(handle: int, out, num_seqs: int, stream=None) -> int:

@@ -67,7 +67,7 @@ class PagedWorkload:
     pin: int = 0
     sm_count: int = 148
     max_decode_seqs: int = 0
-    gqa_pack: bool = False
+    gqa_pack: int = 0            # 0 split-K path, 1 packed (non-split), 2 packed with splits
     seeds: dict = field(default_factory=dict)
 
     @property
@@ -125,6 +125,15 @@ def gqa_packed(seed: int = SEED_VALUES) -> PagedWorkload:
     lens = np.random.default_rng(seed + 1).integers(512, 4096, size=32, endpoint=True)
     return _paged("gqa_packed_32seq_h16kv2_d256", lens, 16, 2, 256, 16, seed + 100,
                   policy="pinned", pin=1, gqa_pack=True)
+
+
+def gqa_packed_splitk(seed: int = SEED_VALUES) -> PagedWorkload:
+    """The GQA-packed workload's sequences through the packed pass with splits
+    (gqa_pack mode 2): Auto at 148 SMs and 16 q heads gives ceil(296 / 16) = 19,
+    clamped to 16 splits."""
+    lens = np.random.default_rng(seed + 1).integers(512, 4096, size=32, endpoint=True)
+    return _paged("gqa_packed_splitk_32seq_h16kv2_d256", lens, 16, 2, 256, 16, seed + 100,
+                  policy="auto", sm_count=148, gqa_pack=2)
 
 
 def long_context(seed: int = SEED_VALUES) -> PagedWorkload:
@@ -254,6 +263,115 @@ def tiled(seed: int = SEED_VALUES, num_seqs: int = 64, num_q_heads: int = 16, nu
                          blocks_per_seq=n, v_pool=vp, seeds={"values": seed, "placement": seed + 401})
 
 
+@dataclass
+class MixedTiledWorkload:
+    """Inputs of one tiled decode step whose step_tile calls read different
+    sources: each sequence's older blocks sit in a paged cache [nb, bs, Hkv, D]
+    (K and V separate), its newer blocks in a scratch pool [slot, K|V, Hkv, bs, D].
+    calls[c] = (source "paged" | "scratch", tile_blocks [S, tcap],
+    tile_block_counts [S], last_block_valid_slots)."""
+
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    tile_capacity: int
+    q: np.ndarray                 # [S, Hq, D] uint16
+    paged_k: np.ndarray           # [nb, bs, Hkv, D] uint16
+    paged_v: np.ndarray
+    scratch: np.ndarray           # [slots, 2, Hkv, bs, D] uint16
+    calls: list
+    blocks_per_seq: np.ndarray    # [S]
+    seeds: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def kv_tokens(self) -> int:
+        bs = self.block_size
+        n = 0
+        for _, _, tc, lb in self.calls:
+            for cnt in tc:
+                if cnt:
+                    n += (int(cnt) - 1) * bs + (lb if 1 <= lb < bs else bs)
+        return n
+
+    @property
+    def kv_bytes(self) -> int:
+        return self.kv_tokens * self.num_kv_heads * self.head_dim * 2 * 2
+
+
+def _right_aligned_calls(ids_per_seq, ncalls: int, tcap: int):
+    """Split each sequence's block list over ncalls tiles of tcap, last tile last."""
+    S = len(ids_per_seq)
+    out = []
+    for c in range(ncalls):
+        tb = np.zeros((S, tcap), dtype=np.int32)
+        tc = np.zeros(S, dtype=np.int32)
+        for s, ids in enumerate(ids_per_seq):
+            n = len(ids)
+            lo = max(0, n - (ncalls - c) * tcap)
+            hi = max(0, n - (ncalls - 1 - c) * tcap)
+            tc[s] = hi - lo
+            tb[s, :hi - lo] = ids[lo:hi]
+        out.append((tb, tc))
+    return out
+
+
+def tiled_mixed(seed: int = SEED_VALUES, num_seqs: int = 64, num_q_heads: int = 16,
+                num_kv_heads: int = 4, head_dim: int = 256, block_size: int = 16,
+                tile_capacity: int = 64, max_blocks: int = 256, last_valid: int = 5,
+                min_zero: int = 2) -> MixedTiledWorkload:
+    """The tiled workload's shape (block counts uniform in [0, 256], at least two
+    sequences with none, Hq 16, Hkv 4, D 256, tiles of 64 blocks) with each
+    sequence's first half of blocks (rounded down) in the paged cache and the rest
+    in the scratch pool.  The step reads the paged source in right-aligned tiles,
+    then the scratch source likewise; only the last call passes
+    last_block_valid_slots = 5, so every non-empty sequence's final block holds 5
+    tokens."""
+    place = np.random.default_rng(seed + 501)
+    n = place.integers(0, max_blocks, size=num_seqs, endpoint=True).astype(np.int64)
+    zeros = int((n == 0).sum())
+    for s in range(num_seqs):
+        if zeros >= min_zero:
+            break
+        if n[s] != 0:
+            n[s] = 0
+            zeros += 1
+    npg = n // 2
+    nsc = n - npg
+    nb = max(1, int(np.ceil(1.25 * int(npg.sum()))))
+    slots = max(1, int(np.ceil(1.25 * int(nsc.sum()))))
+    perm_p = place.permutation(nb).astype(np.int32)
+    perm_s = place.permutation(slots).astype(np.int32)
+    ids_p, ids_s = [], []
+    op = os_ = 0
+    for s in range(num_seqs):
+        ids_p.append(perm_p[op:op + npg[s]])
+        op += npg[s]
+        ids_s.append(perm_s[os_:os_ + nsc[s]])
+        os_ += nsc[s]
+    cp = max(1, -(-int(npg.max()) // tile_capacity)) if len(npg) else 1
+    cs = max(1, -(-int(nsc.max()) // tile_capacity)) if len(nsc) else 1
+    calls = [("paged", tb, tc, block_size) for tb, tc in _right_aligned_calls(ids_p, cp, tile_capacity)]
+    sc = _right_aligned_calls(ids_s, cs, tile_capacity)
+    for c, (tb, tc) in enumerate(sc):
+        calls.append(("scratch", tb, tc, last_valid if c == len(sc) - 1 else block_size))
+    q = normal_bf16((num_seqs, num_q_heads, head_dim), seed * 3 + 500)
+    pk = normal_bf16((nb, block_size, num_kv_heads, head_dim), seed * 3 + 501)
+    pv = normal_bf16((nb, block_size, num_kv_heads, head_dim), seed * 3 + 502)
+    sp = normal_bf16((slots, 2, num_kv_heads, block_size, head_dim), seed * 3 + 503)
+    return MixedTiledWorkload(name=f"tiled_mixed_{num_seqs}seq_h{num_q_heads}kv{num_kv_heads}_d{head_dim}_"
+                                   f"tcap{tile_capacity}",
+                              num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                              block_size=block_size, tile_capacity=tile_capacity, q=q, paged_k=pk,
+                              paged_v=pv, scratch=sp, calls=calls, blocks_per_seq=n,
+                              seeds={"values": seed, "placement": seed + 501})
+
+
 def scratch_pool_views(pool: np.ndarray):
     """Flat K and V views of a scratch pool [slot, 2, Hkv, bs, D]: K starts at element 0,
     V one K|V stripe (Hkv*bs*D elements) later."""
@@ -266,7 +384,9 @@ def scratch_pool_views(pool: np.ndarray):
 WORKLOADS = {
     "tiny": tiny,
     "gqa_packed": gqa_packed,
+    "gqa_packed_splitk": gqa_packed_splitk,
     "long_context": long_context,
     "large_batch": large_batch,
     "tiled": tiled,
+    "tiled_mixed": tiled_mixed,
 }

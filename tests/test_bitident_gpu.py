@@ -174,3 +174,35 @@ def test_ring_depth_does_not_change_bits(cuda_device):
         pd.pd_debug_set_tuning(0, 0, -1)
     for o in outs[1:]:
         assert np.array_equal(outs[0], o)
+
+
+def test_tiled_run_equals_separate_calls(cuda_device):
+    """pd_tiled_run is begin, the steps in order and finalize: same bits as the
+    calls made one by one."""
+    mw = W.tiled_mixed(num_seqs=10, max_blocks=120, seed=8)
+    inp = api.MixedTiledInputs(mw, cuda_device)
+    t = pd.Tiled(mw.num_seqs, mw.num_q_heads, mw.num_kv_heads, mw.head_dim, mw.block_size,
+                 mw.tile_capacity)
+    try:
+        a = api.bf16_bits(api.run_tiled_mixed(inp, t))
+        out = torch.empty((mw.num_seqs, mw.num_q_heads, mw.head_dim), dtype=torch.bfloat16,
+                          device=cuda_device)
+        t.begin(mw.num_seqs)
+        for k, v, tb, tc, st, lb in inp.sources(t):
+            t.step(inp.q, k, v, tb, tc, mw.num_seqs, st, lb)
+        t.finalize(out, mw.num_seqs)
+        torch.cuda.synchronize()
+        assert np.array_equal(a, api.bf16_bits(out))
+    finally:
+        t.close()
+
+
+def test_packed_with_splits_is_batch_invariant(cuda_device):
+    """gqa_pack mode 2 at 16 splits: a sequence's bits alone == in the batch; and
+    mode 2 at one split is the packed pass itself (same bits as mode 1)."""
+    w = W.gqa_packed_splitk()
+    full = _bits(w, cuda_device, 16, pack=2)
+    for s in (0, 9, 31):
+        alone = _bits(_sub_batch(w, [s], relocate_seed=s + 1), cuda_device, 16, pack=2)
+        assert np.array_equal(alone[0], full[s])
+    assert np.array_equal(_bits(w, cuda_device, 1, pack=2), _bits(w, cuda_device, 1, pack=1))

@@ -130,3 +130,33 @@ def test_begin_resets_state(cuda_device):
         assert bool((out == 0).all())
     finally:
         t.close()
+
+
+def test_tiled_run_checks_every_source_before_launching(cuda_device):
+    """A bad source anywhere in the list is reported before anything launches:
+    the running state and the output keep their contents."""
+    mw = W.tiled_mixed(num_seqs=5, num_q_heads=8, num_kv_heads=2, head_dim=64, tile_capacity=4,
+                       max_blocks=16, seed=57)
+    inp = api.MixedTiledInputs(mw, cuda_device)
+    t = pd.Tiled(5, 8, 2, 64, 16, 4)
+    try:
+        good = inp.sources(t)
+        out = torch.full((5, 8, 64), 3.0, dtype=torch.bfloat16, device=cuda_device)
+        bad = list(good)
+        k, v, tb, tc, st, lb = bad[-1]
+        bad[-1] = (k, v, tb, tc, (st[0], 12, st[2]), lb)     # tok stride not a multiple of 8
+        with pytest.raises(pd.PdError) as e:
+            t.run(inp.q, bad, out, 5)
+        assert e.value.code == pd.PD_ERR_INVALID
+        assert "source %d" % (len(bad) - 1) in pd.last_error()
+        torch.cuda.synchronize()
+        assert bool(torch.all(out == 3.0))
+        with pytest.raises(pd.PdError) as e:
+            t.run(inp.q, good, out, 6)                        # above max_seqs
+        assert e.value.code == pd.PD_ERR_CAPACITY
+        # no source: begin then finalize, every output 0
+        t.run(inp.q, [], out, 5)
+        torch.cuda.synchronize()
+        assert bool(torch.all(out == 0))
+    finally:
+        t.close()

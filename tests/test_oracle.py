@@ -285,6 +285,81 @@ def test_scratch_pool_and_paged_layouts_agree():
     assert np.all(got_scratch[zero_seqs] == 0)
 
 
+def _mixed_small(seed=23):
+    return W.tiled_mixed(num_seqs=7, num_q_heads=8, num_kv_heads=2, head_dim=32, tile_capacity=4,
+                         max_blocks=18, seed=seed)
+
+
+def _mixed_calls(mw):
+    kflat, vflat = W.scratch_pool_views(mw.scratch)
+    Hkv, D, bs = mw.num_kv_heads, mw.head_dim, mw.block_size
+    calls = []
+    for kind, tb, tc, lb in mw.calls:
+        if kind == "paged":
+            calls.append(dict(k_pool=mw.paged_k, v_pool=mw.paged_v, tile_blocks=tb, tile_block_counts=tc,
+                              last_block_valid_slots=lb, strides=oracle.paged_strides(Hkv, D, bs)))
+        else:
+            calls.append(dict(k_pool=kflat, v_pool=vflat, tile_blocks=tb, tile_block_counts=tc,
+                              last_block_valid_slots=lb, strides=oracle.scratch_pool_strides(Hkv, D, bs)))
+    return calls
+
+
+def test_tiled_multi_source_matches_torch_sdpa_float64():
+    """One step mixing the paged cache and the scratch pool: the token rows are
+    gathered here by plain array indexing of each layout (no strides), and torch's
+    float64 SDPA over them must agree with the oracle."""
+    mw = _mixed_small()
+    S, Hq, D = mw.q.shape
+    Hkv, bs = mw.num_kv_heads, mw.block_size
+    G = Hq // Hkv
+    want = np.zeros((S, Hq, D))
+    scale = float(np.float32(1 / math.sqrt(D)))
+    for s in range(S):
+        for kvh in range(Hkv):
+            ks, vs = [], []
+            for kind, tb, tc, lb in mw.calls:
+                cnt = int(tc[s])
+                for i in range(cnt):
+                    blk = int(tb[s, i])
+                    ntok = lb if (i == cnt - 1 and 1 <= lb < bs) else bs
+                    for t in range(ntok):
+                        if kind == "paged":
+                            ks.append(mw.paged_k[blk, t, kvh]); vs.append(mw.paged_v[blk, t, kvh])
+                        else:
+                            ks.append(mw.scratch[blk, 0, kvh, t]); vs.append(mw.scratch[blk, 1, kvh, t])
+            if not ks:
+                continue
+            kt = torch.from_numpy(W.bf16_to_f32(np.stack(ks)).astype(np.float64))
+            vt = torch.from_numpy(W.bf16_to_f32(np.stack(vs)).astype(np.float64))
+            qt = torch.from_numpy(W.bf16_to_f32(mw.q[s, kvh * G:(kvh + 1) * G]).astype(np.float64))
+            o = torch.nn.functional.scaled_dot_product_attention(
+                qt[None, :, None, :], kt[None, None].expand(1, G, -1, -1),
+                vt[None, None].expand(1, G, -1, -1), scale=scale)
+            want[s, kvh * G:(kvh + 1) * G] = o[0, :, 0, :].numpy()
+    got = oracle.tiled_attn_multi(mw.q, _mixed_calls(mw), Hkv, bs)
+    assert np.max(np.abs(got - want)) < 1e-12
+    zero = np.where(mw.blocks_per_seq == 0)[0]
+    assert len(zero) >= 1 and np.all(got[zero] == 0)
+    assert sum(1 for c in mw.calls if c[0] == "paged") >= 1
+    assert sum(1 for c in mw.calls if c[0] == "scratch") >= 1
+
+
+def test_tiled_multi_with_one_source_equals_tiled():
+    """Every call naming the same pool and strides is the single-source step."""
+    tw = W.tiled(num_seqs=6, num_q_heads=8, num_kv_heads=2, head_dim=32, tile_capacity=8,
+                 num_calls=3, max_blocks=20, seed=24)
+    kflat, vflat = W.scratch_pool_views(tw.pool)
+    st = oracle.scratch_pool_strides(2, 32, 16)
+    calls = [dict(k_pool=kflat, v_pool=vflat, tile_blocks=tw.tile_blocks[c],
+                  tile_block_counts=tw.tile_block_counts[c],
+                  last_block_valid_slots=int(tw.last_block_valid_slots[c]), strides=st)
+             for c in range(tw.num_calls)]
+    got = oracle.tiled_attn_multi(tw.q, calls, 2, 16)
+    want = oracle.tiled_attn(tw.q, kflat, vflat, tw.tile_blocks, tw.tile_block_counts,
+                             tw.last_block_valid_slots, 2, 16, st)
+    assert np.array_equal(got, want)
+
+
 def test_tolerance_helper():
     assert oracle.bf16_ulp(1.0) == 2.0 ** -7
     assert oracle.bf16_ulp(1.99) == 2.0 ** -7
@@ -317,6 +392,7 @@ MUTATIONS = {
     "token_stride": ("int64_t row = ((blk * block_size + t % block_size) * num_kv_heads + kvh) * head_dim;",
                      "int64_t row = ((blk * block_size + t % block_size) + kvh) * head_dim;"),
     "split_merge_weight": ("double w = exp(m - M);", "double w = exp(M - m);"),
+    "multi_source_tok_stride": ("(int64_t)t * strides[3 * c + 1] +", "(int64_t)t * strides[3 * c + 2] +"),
 }
 
 
@@ -338,7 +414,7 @@ def test_planted_mistake_is_caught(name, monkeypatch):
     try:
         lib = _mutant_lib(name, tmp)
         real = oracle._load()
-        for f in ("orc_decode_attn", "orc_split_replay", "orc_tiled_attn"):
+        for f in ("orc_decode_attn", "orc_split_replay", "orc_tiled_attn", "orc_tiled_attn_multi"):
             getattr(lib, f).argtypes = getattr(real, f).argtypes
             getattr(lib, f).restype = getattr(real, f).restype
         monkeypatch.setattr(oracle, "_lib", lib)
@@ -346,6 +422,7 @@ def test_planted_mistake_is_caught(name, monkeypatch):
             lambda: test_matches_torch_sdpa_float64(*SDPA_CASES[1]),
             lambda: test_dominant_key_selects_its_value(4000.0),
             lambda: test_split_replay_matches_direct_for_every_split_count(16),
+            lambda: test_tiled_multi_source_matches_torch_sdpa_float64(),
         ]
         failed = 0
         for pin in pins:

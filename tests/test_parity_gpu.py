@@ -155,3 +155,74 @@ def test_split_geometry_matches_oracle_policy():
     for L in (0, 1, 255, 256, 257, 32768):
         for n in (1, 3, 13):
             assert pd.pd_split_chunk_tokens(L, n, 16) == P.split_chunk_tokens(L, n, 16)
+
+
+def _mixed_ref(mw):
+    kflat, vflat = W.scratch_pool_views(mw.scratch)
+    Hkv, D, bs = mw.num_kv_heads, mw.head_dim, mw.block_size
+    calls = []
+    for kind, tb, tc, lb in mw.calls:
+        if kind == "paged":
+            calls.append(dict(k_pool=mw.paged_k, v_pool=mw.paged_v, tile_blocks=tb, tile_block_counts=tc,
+                              last_block_valid_slots=lb, strides=oracle.paged_strides(Hkv, D, bs)))
+        else:
+            calls.append(dict(k_pool=kflat, v_pool=vflat, tile_blocks=tb, tile_block_counts=tc,
+                              last_block_valid_slots=lb, strides=oracle.scratch_pool_strides(Hkv, D, bs)))
+    return oracle.tiled_attn_multi(mw.q, calls, Hkv, bs)
+
+
+def test_tiled_mixed_sources_full_size(cuda_device):
+    """pd_tiled_run over the paged cache then the scratch pool (tiled_attention.rs
+    page: step_tile takes its pools and strides per call), 64 sequences."""
+    mw = W.tiled_mixed()
+    got = api.bf16_to_f64(api.run_tiled_mixed(api.MixedTiledInputs(mw, cuda_device)))
+    assert pd.pd_device_status() == 0
+    ref = _mixed_ref(mw)
+    assert_within_tolerance(got, ref, "tiled mixed sources")
+    zero = np.where(mw.blocks_per_seq == 0)[0]
+    assert len(zero) >= 2 and np.all(got[zero] == 0.0)
+
+
+@pytest.mark.parametrize("G,D,tcap", [(1, 64, 3), (3, 128, 8), (8, 256, 5)])
+def test_tiled_mixed_sources_shapes(cuda_device, G, D, tcap):
+    mw = W.tiled_mixed(num_seqs=9, num_q_heads=2 * G, num_kv_heads=2, head_dim=D, tile_capacity=tcap,
+                       max_blocks=30, last_valid=7, seed=6)
+    got = api.bf16_to_f64(api.run_tiled_mixed(api.MixedTiledInputs(mw, cuda_device)))
+    assert_within_tolerance(got, _mixed_ref(mw), f"tiled mixed G{G} D{D}")
+
+
+def test_gqa_packed_splitk_full_size(cuda_device):
+    """The packed pass with splits (gqa_pack mode 2): the packed workload's
+    sequences at Auto's 16 splits, partials through the workspace and the merge."""
+    w = W.gqa_packed_splitk()
+    inp = api.PagedInputs(w, cuda_device)
+    n = inp.splits()
+    assert n == 16
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    assert_within_tolerance(_run(w, cuda_device, num_splits=n, gqa_pack=2), ref, "gqa_packed splitk")
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 16])
+def test_gqa_packed_splitk_ragged(cuda_device, N):
+    w = W.custom([0, 1, 16, 17, 255, 256, 257, 700, 2500, 4097], 16, 2, 256, seed=34)
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    got = _run(w, cuda_device, num_splits=N, gqa_pack=2)
+    assert_within_tolerance(got, ref, f"packed splitk N={N}")
+    assert np.all(got[0] == 0.0)
+
+
+def test_gqa_packed_splitk_shape_gate(cuda_device):
+    import torch
+    w = W.custom([300], 8, 2, 256, seed=35)  # group 4: not the packed shape
+    inp = api.PagedInputs(w, cuda_device)
+    out = torch.full((1, 8, 256), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    ws = api.workspace(1, 8, 256, 4, cuda_device)
+    rc = pd.pd_decode_attn(inp.q, inp.k, inp.v, inp.block_table, inp.context_lens, out, w.inv_sqrt_d,
+                           4, ws, pd.PD_GQA_PACK_SPLITK)
+    assert rc == pd.PD_NOT_APPLICABLE
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
+    with pytest.raises(pd.PdError) as e:
+        pd.pd_decode_attn(inp.q, inp.k, inp.v, inp.block_table, inp.context_lens, out, w.inv_sqrt_d,
+                          1, None, 3)
+    assert e.value.code == pd.PD_ERR_INVALID
