@@ -64,8 +64,12 @@ def _load():
                                            i32, i64, i64, i64, p]
             lib.orc_tiled_attn_multi.argtypes = [p, p, p, p, p, p, p, p, p, i32, i32, i32, i32,
                                                  i32, i32, p]
+            lib.orc_decode_attn_fp8.argtypes = [p, p, p, ctypes.c_float, ctypes.c_float, p, i64, p,
+                                                i32, i32, i32, i32, i32, i64, ctypes.c_float, p]
+            lib.orc_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_value.restype = ctypes.c_double
             for f in (lib.orc_decode_attn, lib.orc_split_replay, lib.orc_tiled_attn,
-                      lib.orc_tiled_attn_multi):
+                      lib.orc_tiled_attn_multi, lib.orc_decode_attn_fp8):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -148,6 +152,34 @@ def tiled_attn(q, k_pool, v_pool, tile_blocks, tile_block_counts, last_block_val
                                 _ptr(tc), _ptr(lb), T, S, Hq, num_kv_heads, D, block_size, tcap,
                                 blk, tok, kvh, _ptr(out))
     _check(rc, "tiled_attn")
+    return out
+
+
+def e4m3_values() -> np.ndarray:
+    """The value of every FP8 E4M3 code 0..255 (NaN for the two NaN codes), FP64."""
+    lib = _load()
+    return np.array([lib.orc_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def decode_attn_fp8(q, k_cache, v_cache, k_scale: float, v_scale: float, block_table, context_lens,
+                    inv_sqrt_d: float) -> np.ndarray:
+    """Paged-decode attention by definition over an FP8 E4M3 KV cache, FP64.
+
+    k_cache / v_cache [num_blocks, block_size, Hkv, D] uint8 E4M3 codes; K and V
+    are code value * k_scale / v_scale (per-tensor FP32 scales); q BF16 bits.
+    """
+    q = _u16(q)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    bt, cl = _i32(block_table), _i32(context_lens)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, D2 = kc.shape
+    assert D2 == D and vc.shape == kc.shape and bt.shape[0] == S and cl.shape == (S,)
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    rc = _load().orc_decode_attn_fp8(_ptr(q), _ptr(kc), _ptr(vc), float(k_scale), float(v_scale),
+                                     _ptr(bt), bt.shape[1], _ptr(cl), S, Hq, Hkv, D, bs, nb,
+                                     float(inv_sqrt_d), _ptr(out))
+    _check(rc, "decode_attn_fp8")
     return out
 
 

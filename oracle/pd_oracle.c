@@ -43,6 +43,13 @@
  *   pools and strides (the page's step_tile takes them per call, so one step
  *   may mix the paged layout and the scratch-pool layout).
  *
+ *   orc_decode_attn_fp8 is the paged definition over an FP8 KV cache (the
+ *   Module attn_splitk page names BF16 and FP8 paged-decode launches but no
+ *   format or scale).  Reading: OCP FP8 E4M3 (sign, 4 exponent bits with bias
+ *   7, 3 mantissa bits; no infinities; exponent 15 with mantissa 7 is NaN),
+ *   one FP32 scale per tensor: K = e4m3(k_code) * k_scale, V = e4m3(v_code)
+ *   * v_scale, both formed exactly in FP64; then the definition above.
+ *
  * Return codes: 0 ok, -1 bad argument, -2 out of memory, -3 a block id or
  * context length outside the buffers the caller described.
  */
@@ -445,6 +452,112 @@ int orc_tiled_attn_multi(const uint16_t *q, const uint16_t *const *k_pools,
 done:
     free(krows);
     free(vrows);
+    free(x);
+    return rc;
+}
+
+/* OCP FP8 E4M3 code -> value (exact in FP64). */
+double orc_e4m3_value(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);                  /* m/8 * 2^-6 */
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * Paged-decode attention by definition over an FP8 E4M3 cache with per-tensor
+ * scales.  q [num_seqs, Hq, D] BF16 bits; k_cache, v_cache
+ * [num_blocks, block_size, Hkv, D] E4M3 codes; the rest as orc_decode_attn.
+ */
+int orc_decode_attn_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                        float k_scale, float v_scale, const int32_t *block_table,
+                        int64_t max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        int64_t num_blocks, float inv_sqrt_d, double *out)
+{
+    if (check_heads(num_q_heads, num_kv_heads, head_dim, block_size) != 0 || num_seqs < 0)
+        return -1;
+    for (int s = 0; s < num_seqs; ++s)
+        if (context_lens[s] < 0)
+            return -3;
+    int64_t lmax = max_context(context_lens, num_seqs);
+    double *kr = malloc(sizeof(double) * (size_t)((lmax + 1) * head_dim));
+    double *vr = malloc(sizeof(double) * (size_t)((lmax + 1) * head_dim));
+    double *qd = malloc(sizeof(double) * (size_t)head_dim);
+    double *x = malloc(sizeof(double) * (size_t)(lmax + 1));
+    int rc = 0;
+    if (!kr || !vr || !qd || !x) {
+        rc = -2;
+        goto done;
+    }
+    int G = num_q_heads / num_kv_heads;
+    double scale = (double)inv_sqrt_d;
+    double ks = (double)k_scale, vs = (double)v_scale;
+    for (int s = 0; s < num_seqs && rc == 0; ++s) {
+        int64_t L = context_lens[s];
+        for (int kvh = 0; kvh < num_kv_heads && rc == 0; ++kvh) {
+            /* the sequence's K and V rows for this KV head, dequantised */
+            for (int64_t t = 0; t < L; ++t) {
+                int64_t j = t / block_size;
+                if (j >= max_blocks_per_seq) {
+                    rc = -3;
+                    break;
+                }
+                int64_t blk = block_table[(int64_t)s * max_blocks_per_seq + j];
+                if (blk < 0 || blk >= num_blocks) {
+                    rc = -3;
+                    break;
+                }
+                int64_t row = ((blk * block_size + t % block_size) * num_kv_heads + kvh) * head_dim;
+                for (int d = 0; d < head_dim; ++d) {
+                    kr[t * head_dim + d] = orc_e4m3_value(k_cache[row + d]) * ks;
+                    vr[t * head_dim + d] = orc_e4m3_value(v_cache[row + d]) * vs;
+                }
+            }
+            if (rc != 0)
+                break;
+            for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
+                const uint16_t *qrow = q + ((int64_t)s * num_q_heads + h) * head_dim;
+                double *o = out + ((int64_t)s * num_q_heads + h) * head_dim;
+                for (int d = 0; d < head_dim; ++d) {
+                    qd[d] = widen_bf16(qrow[d]);
+                    o[d] = 0.0;
+                }
+                if (L == 0)
+                    continue; /* l = 0  ->  output 0 */
+                double xmax = -INFINITY;
+                for (int64_t t = 0; t < L; ++t) {
+                    double acc = 0.0;
+                    for (int d = 0; d < head_dim; ++d)
+                        acc += qd[d] * kr[t * head_dim + d];
+                    x[t] = scale * acc;
+                    if (x[t] > xmax)
+                        xmax = x[t];
+                }
+                double den = 0.0;
+                for (int64_t t = 0; t < L; ++t) {
+                    double w = exp(x[t] - xmax);
+                    den += w;
+                    for (int d = 0; d < head_dim; ++d)
+                        o[d] += w * vr[t * head_dim + d];
+                }
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] /= den;
+            }
+        }
+    }
+done:
+    free(kr);
+    free(vr);
+    free(qd);
     free(x);
     return rc;
 }

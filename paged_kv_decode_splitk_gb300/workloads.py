@@ -69,6 +69,9 @@ class PagedWorkload:
     max_decode_seqs: int = 0
     gqa_pack: int = 0            # 0 split-K path, 1 packed (non-split), 2 packed with splits
     seeds: dict = field(default_factory=dict)
+    kv_dtype: str = "bf16"       # "bf16": k/v_cache hold BF16 bits; "e4m3": FP8 E4M3 codes (uint8)
+    k_scale: float = 1.0         # e4m3 only: K = code value * k_scale, V = code value * v_scale
+    v_scale: float = 1.0
 
     @property
     def num_seqs(self) -> int:
@@ -79,9 +82,14 @@ class PagedWorkload:
         return int(self.k_cache.shape[0])
 
     @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.kv_dtype == "e4m3" else 2
+
+    @property
     def kv_bytes(self) -> int:
         """Algorithmic K+V bytes of one launch: live tokens only."""
-        return int(self.context_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 2 * 2
+        return (int(self.context_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim
+                * self.kv_elem_bytes * 2)
 
 
 def _paged(name, lens, num_q_heads, num_kv_heads, head_dim, block_size, seed, pool_factor=1.25,
@@ -155,6 +163,57 @@ def large_batch(seed: int = SEED_VALUES, num_seqs: int = 256) -> PagedWorkload:
     lens = large_batch_lens(num_seqs, seed)
     return _paged(f"large_batch_{num_seqs}seq_h32kv8_d128", lens, 32, 8, 128, 16, seed + 300,
                   policy="auto", sm_count=148)
+
+
+def e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """Round FP32 values to FP8 E4M3 (nearest, ties to even, as torch's float8_e4m3fn
+    cast does); returns the uint8 codes.  Inputs must lie within +-448."""
+    import torch
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert np.all(np.abs(x) <= 448.0), "outside the E4M3 range"
+    return torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def fp8_variant(w: PagedWorkload, k_scale: float = 0.5, v_scale: float = 0.25,
+                seed: int = SEED_VALUES) -> PagedWorkload:
+    """The same shape, sequences and block table with an FP8 E4M3 KV cache: fresh
+    N(0, 1) draws divided by the per-tensor scale and rounded to E4M3 (so the
+    dequantised cache is again about N(0, 1); about 1% of the codes are subnormal)."""
+    shape = w.k_cache.shape
+    n = int(np.prod(shape))
+    out = []
+    for i, sc in enumerate((k_scale, v_scale)):
+        rng = np.random.default_rng(20_000 + seed * 3 + i)
+        vals = np.empty(n, dtype=np.uint8)
+        chunk = 1 << 24
+        for a in range(0, n, chunk):
+            b = min(n, a + chunk)
+            vals[a:b] = e4m3_codes(np.clip(rng.standard_normal(b - a, dtype=np.float32) / np.float32(sc),
+                                           -448.0, 448.0))
+        out.append(vals.reshape(shape))
+    kw = dict(w.__dict__)
+    kw.update(name=w.name + "_e4m3", k_cache=out[0], v_cache=out[1], kv_dtype="e4m3",
+              k_scale=float(np.float32(k_scale)), v_scale=float(np.float32(v_scale)))
+    kw["seeds"] = dict(w.seeds, fp8=seed)
+    return PagedWorkload(**kw)
+
+
+def long_context_fp8(seed: int = SEED_VALUES) -> PagedWorkload:
+    """The long-context workload (1 x 32768 tokens, Hq 24, Hkv 8, D 128, 13 splits)
+    over an FP8 E4M3 cache with k_scale 0.5, v_scale 0.25."""
+    return fp8_variant(long_context(seed), seed=seed)
+
+
+def large_batch_fp8(seed: int = SEED_VALUES) -> PagedWorkload:
+    """The large-batch workload (256 lognormal sequences, Hq 32, Hkv 8, D 128, 10
+    splits) over an FP8 E4M3 cache with k_scale 0.5, v_scale 0.25."""
+    return fp8_variant(large_batch(seed), seed=seed)
+
+
+def gqa_packed_fp8(seed: int = SEED_VALUES) -> PagedWorkload:
+    """The GQA-packed workload (32 sequences, Hq 16, Hkv 2, D 256, packed, non-split)
+    over an FP8 E4M3 cache with k_scale 0.5, v_scale 0.25."""
+    return fp8_variant(gqa_packed(seed), seed=seed)
 
 
 def custom(lens, num_q_heads, num_kv_heads, head_dim, block_size=16, seed=SEED_VALUES,
@@ -385,6 +444,9 @@ WORKLOADS = {
     "tiny": tiny,
     "gqa_packed": gqa_packed,
     "gqa_packed_splitk": gqa_packed_splitk,
+    "gqa_packed_fp8": gqa_packed_fp8,
+    "long_context_fp8": long_context_fp8,
+    "large_batch_fp8": large_batch_fp8,
     "long_context": long_context,
     "large_batch": large_batch,
     "tiled": tiled,

@@ -360,6 +360,76 @@ def test_tiled_multi_with_one_source_equals_tiled():
     assert np.array_equal(got, want)
 
 
+def test_e4m3_decoding_matches_torch_float8():
+    """Every FP8 E4M3 code against torch's float8_e4m3fn (a library routine)."""
+    got = oracle.e4m3_values()
+    want = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert int(np.isnan(got).sum()) == 2 and np.nanmax(got) == 448.0 and got[1] == 2.0 ** -9
+
+
+def _fp8_contiguous(lens, Hq, Hkv, D, seed, ks, vs):
+    q, k, v, bt, cl, starts = _contiguous_workload(lens, Hq, Hkv, D, 16, seed)
+    rng = np.random.default_rng(seed)
+    k8 = W.e4m3_codes(rng.standard_normal(k.shape).astype(np.float32) / np.float32(ks))
+    v8 = W.e4m3_codes(rng.standard_normal(v.shape).astype(np.float32) / np.float32(vs))
+    return q, k8, v8, bt, cl, starts
+
+
+@pytest.mark.parametrize("ks,vs", [(0.5, 0.25), (0.37, 1.7)])
+def test_fp8_attention_matches_torch_sdpa_float64(ks, vs):
+    """FP8 cache: torch float8 decode times the scale, then torch SDPA in float64."""
+    lens, Hq, Hkv, D = [1, 15, 16, 17, 70], 8, 2, 32
+    q, k8, v8, bt, cl, starts = _fp8_contiguous(lens, Hq, Hkv, D, 61, ks, vs)
+    f8 = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64)
+    kf = (f8(k8) * float(np.float32(ks))).reshape(-1, Hkv, D)
+    vf = (f8(v8) * float(np.float32(vs))).reshape(-1, Hkv, D)
+    qf = torch.from_numpy(W.bf16_to_f32(q).astype(np.float64))
+    scale = float(np.float32(1 / math.sqrt(D)))
+    G = Hq // Hkv
+    want = np.zeros((len(lens), Hq, D))
+    for s, L in enumerate(lens):
+        kk = kf[starts[s]:starts[s] + L].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        vv = vf[starts[s]:starts[s] + L].permute(1, 0, 2).repeat_interleave(G, dim=0)
+        o = torch.nn.functional.scaled_dot_product_attention(qf[s].unsqueeze(1)[None], kk[None], vv[None],
+                                                             scale=scale)
+        want[s] = o[0, :, 0, :].numpy()
+    got = oracle.decode_attn_fp8(q, k8, v8, ks, vs, bt, cl, scale)
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+def test_fp8_equals_bf16_definition_on_exact_values():
+    """With power-of-two scales every dequantised value is a BF16 value: the FP8
+    oracle must equal the BF16 oracle on those values, bit for bit."""
+    w = W.custom([0, 5, 33, 160], 8, 2, 64, seed=62)
+    w8 = W.fp8_variant(w, k_scale=0.5, v_scale=4.0, seed=3)
+    val = oracle.e4m3_values()
+    kb = W.bf16_bits((val[w8.k_cache] * 0.5).astype(np.float32))
+    vb = W.bf16_bits((val[w8.v_cache] * 4.0).astype(np.float32))
+    assert np.array_equal(W.bf16_to_f32(kb).astype(np.float64), val[w8.k_cache] * 0.5)
+    got = oracle.decode_attn_fp8(w8.q, w8.k_cache, w8.v_cache, 0.5, 4.0, w8.block_table, w8.context_lens,
+                                 w8.inv_sqrt_d)
+    want = oracle.decode_attn(w8.q, kb, vb, w8.block_table, w8.context_lens, w8.inv_sqrt_d)
+    assert np.array_equal(got, want)
+    assert np.all(got[0] == 0.0)
+
+
+def test_fp8_scales_fold_into_the_softmax_scale_and_the_output():
+    """K scale a with softmax scale b == K scale 1 with scale a*b; V scale c scales
+    the output by c (closed forms of the definition)."""
+    w8 = W.fp8_variant(W.custom([40, 77], 8, 2, 64, seed=63), seed=4)
+    base = oracle.decode_attn_fp8(w8.q, w8.k_cache, w8.v_cache, 1.0, 1.0, w8.block_table, w8.context_lens,
+                                  0.125)
+    a = oracle.decode_attn_fp8(w8.q, w8.k_cache, w8.v_cache, 2.0, 1.0, w8.block_table, w8.context_lens,
+                               0.0625)
+    assert np.array_equal(a, base)
+    c = oracle.decode_attn_fp8(w8.q, w8.k_cache, w8.v_cache, 1.0, 3.0, w8.block_table, w8.context_lens,
+                               0.125)
+    assert np.max(np.abs(c - 3.0 * base)) < 1e-13
+
+
 def test_tolerance_helper():
     assert oracle.bf16_ulp(1.0) == 2.0 ** -7
     assert oracle.bf16_ulp(1.99) == 2.0 ** -7
@@ -393,6 +463,10 @@ MUTATIONS = {
                      "int64_t row = ((blk * block_size + t % block_size) + kvh) * head_dim;"),
     "split_merge_weight": ("double w = exp(m - M);", "double w = exp(M - m);"),
     "multi_source_tok_stride": ("(int64_t)t * strides[3 * c + 1] +", "(int64_t)t * strides[3 * c + 2] +"),
+    "e4m3_bias": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3_subnormal": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    "fp8_v_scale": ("vr[t * head_dim + d] = orc_e4m3_value(v_cache[row + d]) * vs;",
+                    "vr[t * head_dim + d] = orc_e4m3_value(v_cache[row + d]) * ks;"),
 }
 
 
@@ -414,7 +488,8 @@ def test_planted_mistake_is_caught(name, monkeypatch):
     try:
         lib = _mutant_lib(name, tmp)
         real = oracle._load()
-        for f in ("orc_decode_attn", "orc_split_replay", "orc_tiled_attn", "orc_tiled_attn_multi"):
+        for f in ("orc_decode_attn", "orc_split_replay", "orc_tiled_attn", "orc_tiled_attn_multi",
+                  "orc_decode_attn_fp8", "orc_e4m3_value"):
             getattr(lib, f).argtypes = getattr(real, f).argtypes
             getattr(lib, f).restype = getattr(real, f).restype
         monkeypatch.setattr(oracle, "_lib", lib)
@@ -423,6 +498,8 @@ def test_planted_mistake_is_caught(name, monkeypatch):
             lambda: test_dominant_key_selects_its_value(4000.0),
             lambda: test_split_replay_matches_direct_for_every_split_count(16),
             lambda: test_tiled_multi_source_matches_torch_sdpa_float64(),
+            lambda: test_e4m3_decoding_matches_torch_float8(),
+            lambda: test_fp8_attention_matches_torch_sdpa_float64(0.37, 1.7),
         ]
         failed = 0
         for pin in pins:
