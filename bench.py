@@ -157,7 +157,7 @@ def run_ours(args):
     if not tiled:
         base = api.PagedInputs(w, dev)
         n = base.splits()
-        pool_bytes = base.k.numel() * 2 * 2
+        pool_bytes = base.k.numel() * base.k.element_size() * 2
         copies = max(2, -(-3 * L2_BYTES // pool_bytes))
         ks = [base.k] + [base.k.clone() for _ in range(copies - 1)]
         vs = [base.v] + [base.v.clone() for _ in range(copies - 1)]
@@ -167,7 +167,7 @@ def run_ours(args):
 
         def step(i):
             api.decode_attn(base.q, ks[i % copies], vs[i % copies], base.block_table, base.context_lens,
-                            w.inv_sqrt_d, n, w.gqa_pack, out, wsp)
+                            w.inv_sqrt_d, n, w.gqa_pack, out, wsp, None, w.k_scale, w.v_scale)
         l2_note = f"rotating {copies} KV-cache copies ({copies * pool_bytes / 1e6:.0f} MB > 129 MB L2)"
     elif mixed:
         # one pd_tiled_run per step: begin, the paged-cache calls, the scratch-pool
@@ -306,7 +306,7 @@ def run_ours(args):
                 dk.copy_(hk, non_blocking=True)
                 dv.copy_(hv, non_blocking=True)
             api.decode_attn(dq, dk if upload_kv else ks[0], dv if upload_kv else vs[0], dbt, dcl,
-                            w.inv_sqrt_d, n, w.gqa_pack, out, wsp)
+                            w.inv_sqrt_d, n, w.gqa_pack, out, wsp, None, w.k_scale, w.v_scale)
             hout.copy_(out, non_blocking=True)
 
         def timed(upload_kv, k):
@@ -328,7 +328,7 @@ def run_ours(args):
         ms_res = timed(False, max(3, min(args.steps, 2000)))
         e2e = {"value": round(ws * kv_bytes / (ms_kv / 1e3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(ms_kv, 5),
-               "h2d_bytes_per_step": int(small_in + hk.numel() * 2 + hv.numel() * 2),
+               "h2d_bytes_per_step": int(small_in + (hk.numel() + hv.numel()) * hk.element_size()),
                "d2h_bytes_per_step": int(out_b),
                "note": "host buffers: q, block table, context lengths and the whole K/V pool copied "
                        "from pinned host memory every step, output read back"}
@@ -369,6 +369,7 @@ def run_ours(args):
                 "block_size": w.block_size,
                 "num_splits": n,
                 "gqa_pack": int(w.__dict__.get("gqa_pack", 0)),
+                "kv_dtype": w.__dict__.get("kv_dtype", "bf16"),
                 "kv_bytes_per_step": kv_bytes,
                 "tokens": int(w.context_lens.sum()) if not tiled else w.kv_tokens,
                 "l2": l2_note,
@@ -400,6 +401,9 @@ def run_ours(args):
 
 def _oracle_step(w, seqs):
     import oracle
+    if getattr(w, "kv_dtype", "bf16") == "e4m3":
+        return oracle.decode_attn_fp8(w.q[seqs], w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                      w.block_table[seqs], w.context_lens[seqs], w.inv_sqrt_d)
     if hasattr(w, "context_lens"):
         return oracle.decode_attn(w.q[seqs], w.k_cache, w.v_cache, w.block_table[seqs],
                                   w.context_lens[seqs], w.inv_sqrt_d)
@@ -423,7 +427,8 @@ def _oracle_step(w, seqs):
 
 def _seq_bytes(w, seqs):
     if hasattr(w, "context_lens"):
-        return int(w.context_lens[seqs].astype("int64").sum()) * w.num_kv_heads * w.head_dim * 4
+        return (int(w.context_lens[seqs].astype("int64").sum()) * w.num_kv_heads * w.head_dim * 2
+                * w.kv_elem_bytes)
     bs = w.block_size
     tok = 0
     if hasattr(w, "calls"):
@@ -520,7 +525,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_packed",
                     choices=["tiny", "gqa_packed", "gqa_packed_splitk", "long_context", "large_batch", "tiled",
-                             "tiled_mixed"])
+                             "tiled_mixed", "gqa_packed_fp8", "long_context_fp8", "large_batch_fp8"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

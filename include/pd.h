@@ -209,6 +209,26 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
                    float inv_sqrt_d, int num_splits, void *workspace, size_t workspace_bytes,
                    int gqa_pack, void *stream);
 
+/* Paged-decode attention over an FP8 KV cache (Module attn_splitk page: the
+ * dispatch serves "BF16 and FP8" paged-decode launches; the page gives no
+ * format or scale, so this build reads it as OCP FP8 E4M3 codes with one FP32
+ * scale per tensor).
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim] E4M3
+ *                     codes (1 byte each), 16-B aligned; the keys and values
+ *                     are code value * k_scale and code value * v_scale.
+ *   k_scale, v_scale  finite FP32 scales.
+ * Every other argument, the split geometry, the packed modes, the workspace
+ * and the output are those of pd_decode_attn (q stays BF16, out is BF16).
+ * head_dim must be a multiple of 16 (PD_ERR_UNSUPPORTED otherwise).  The two
+ * E4M3 NaN codes are not valid cache contents.
+ * Returns PD_OK, PD_NOT_APPLICABLE, PD_ERR_INVALID, PD_ERR_WORKSPACE,
+ * PD_ERR_UNSUPPORTED or PD_ERR_CUDA. */
+int pd_decode_attn_fp8(const void *q, const void *k_cache, const void *v_cache, float k_scale,
+                       float v_scale, const int32_t *block_table, int max_blocks_per_seq,
+                       const int32_t *context_lens, void *out, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks, float inv_sqrt_d,
+                       int num_splits, void *workspace, size_t workspace_bytes, int gqa_pack, void *stream);
+
 /* Size of the library-owned split-K workspace behind pd_decode_attn_noalloc. */
 #define PD_NOALLOC_WORKSPACE_BYTES 16777216u /* 16 MiB */
 

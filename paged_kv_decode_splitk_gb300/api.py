@@ -38,8 +38,12 @@ class PagedInputs:
         self.w = w
         self.device = torch.device(device)
         self.q = bf16_tensor(w.q, self.device)
-        self.k = bf16_tensor(w.k_cache, self.device)
-        self.v = bf16_tensor(w.v_cache, self.device)
+        if getattr(w, "kv_dtype", "bf16") == "e4m3":   # FP8 E4M3 codes, one byte each
+            self.k = torch.from_numpy(np.ascontiguousarray(w.k_cache, dtype=np.uint8)).to(self.device)
+            self.v = torch.from_numpy(np.ascontiguousarray(w.v_cache, dtype=np.uint8)).to(self.device)
+        else:
+            self.k = bf16_tensor(w.k_cache, self.device)
+            self.v = bf16_tensor(w.v_cache, self.device)
         self.block_table = i32_tensor(w.block_table, self.device)
         self.context_lens = i32_tensor(w.context_lens, self.device)
 
@@ -60,16 +64,22 @@ def workspace(num_seqs: int, num_q_heads: int, head_dim: int, num_splits: int, d
 
 
 def decode_attn(q, k_cache, v_cache, block_table, context_lens, inv_sqrt_d: float, num_splits: int,
-                gqa_pack: bool = False, out=None, ws=None, stream=None):
+                gqa_pack: int = 0, out=None, ws=None, stream=None, k_scale: float = 1.0,
+                v_scale: float = 1.0):
     """Paged-decode attention; returns out [S, Hq, D] BF16 (or None when the packed
-    pass does not apply to the shape, mirroring PD_NOT_APPLICABLE)."""
+    pass does not apply to the shape, mirroring PD_NOT_APPLICABLE).  uint8 caches
+    are FP8 E4M3 codes with per-tensor scales k_scale / v_scale."""
     S, Hq, D = q.shape
     if out is None:
         out = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=q.device)
     if ws is None and num_splits > 1:
         ws = workspace(S, Hq, D, num_splits, q.device)
-    rc = pd.pd_decode_attn(q, k_cache, v_cache, block_table, context_lens, out, inv_sqrt_d,
-                           num_splits, ws, gqa_pack, stream)
+    if k_cache.dtype == torch.uint8:
+        rc = pd.pd_decode_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens, out,
+                                   inv_sqrt_d, num_splits, ws, gqa_pack, stream)
+    else:
+        rc = pd.pd_decode_attn(q, k_cache, v_cache, block_table, context_lens, out, inv_sqrt_d,
+                               num_splits, ws, gqa_pack, stream)
     if rc == pd.PD_NOT_APPLICABLE:
         return None
     return out
@@ -81,7 +91,7 @@ def run_paged(inp: PagedInputs, num_splits: int | None = None, gqa_pack: bool | 
     n = inp.splits() if num_splits is None else num_splits
     pack = w.gqa_pack if gqa_pack is None else gqa_pack
     return decode_attn(inp.q, inp.k, inp.v, inp.block_table, inp.context_lens, w.inv_sqrt_d, n,
-                       pack, out, ws, stream)
+                       pack, out, ws, stream, getattr(w, "k_scale", 1.0), getattr(w, "v_scale", 1.0))
 
 
 class TiledInputs:

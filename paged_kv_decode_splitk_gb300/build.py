@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpd.so")
 
 SOURCES = ["pd_api.cu", "pd_small.cu", "pd_unit_d64.cu", "pd_unit_d128.cu", "pd_unit_d256.cu",
-           "pd_noalloc.cu"]
+           "pd_unit_fp8_d64.cu", "pd_unit_fp8_d128.cu", "pd_unit_fp8_d256.cu", "pd_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

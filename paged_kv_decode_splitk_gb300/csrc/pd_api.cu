@@ -127,12 +127,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 // else), so repeated launches over the same cache skip the host-side encode.
 struct KvMapKey {
     const void *base;
-    int head_dim, block_size, num_kv_heads;
+    int head_dim, block_size, num_kv_heads, elem, box_cols;
     long long num_blocks, blk_stride, tok_stride, kvh_stride;
     bool operator==(const KvMapKey &o) const {
         return base == o.base && head_dim == o.head_dim && block_size == o.block_size &&
-               num_kv_heads == o.num_kv_heads && num_blocks == o.num_blocks &&
-               blk_stride == o.blk_stride && tok_stride == o.tok_stride && kvh_stride == o.kvh_stride;
+               num_kv_heads == o.num_kv_heads && elem == o.elem && box_cols == o.box_cols &&
+               num_blocks == o.num_blocks && blk_stride == o.blk_stride && tok_stride == o.tok_stride &&
+               kvh_stride == o.kvh_stride;
     }
 };
 struct KvMapEntry {
@@ -148,13 +149,17 @@ unsigned long long g_map_clock = 0;
 
 int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int head_dim,
                            int block_size, int num_kv_heads, long long num_blocks,
-                           long long blk_stride, long long tok_stride, long long kvh_stride);
+                           long long blk_stride, long long tok_stride, long long kvh_stride, int elem,
+                           int box_cols);
 
+// 4-D tensor map of a K or V view (strides in elements).  elem 2: BF16, boxes
+// of 64 columns with the 128-byte swizzle; elem 1: FP8 E4M3 codes, one
+// unswizzled box of box_cols columns (the padded head dim) per tile.
 int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim, int block_size,
                   int num_kv_heads, long long num_blocks, long long blk_stride, long long tok_stride,
-                  long long kvh_stride) {
-    const KvMapKey key = {base, head_dim, block_size, num_kv_heads, num_blocks, blk_stride, tok_stride,
-                          kvh_stride};
+                  long long kvh_stride, int elem = 2, int box_cols = pd::kBoxCols) {
+    const KvMapKey key = {base, head_dim, block_size, num_kv_heads, elem, box_cols, num_blocks, blk_stride,
+                          tok_stride, kvh_stride};
     std::lock_guard<std::mutex> lock(g_map_mu);
     int victim = 0;
     for (int i = 0; i < kMapCache; ++i) {
@@ -167,7 +172,7 @@ int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim
         if (g_maps[i].stamp < g_maps[victim].stamp) victim = i;
     }
     int rc = encode_kv_map_uncached(map, tok_dim, base, head_dim, block_size, num_kv_heads, num_blocks,
-                                    blk_stride, tok_stride, kvh_stride);
+                                    blk_stride, tok_stride, kvh_stride, elem, box_cols);
     if (rc != PD_OK) return rc;
     g_maps[victim].key = key;
     g_maps[victim].map = *map;
@@ -178,7 +183,8 @@ int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim
 
 int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int head_dim,
                            int block_size, int num_kv_heads, long long num_blocks,
-                           long long blk_stride, long long tok_stride, long long kvh_stride) {
+                           long long blk_stride, long long tok_stride, long long kvh_stride, int elem,
+                           int box_cols) {
     auto enc = encoder();
     if (!enc) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled entry point");
     const bool tok_first = tok_stride <= kvh_stride;
@@ -187,27 +193,28 @@ int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int
     cuuint32_t box[4];
     cuuint32_t estr[4] = {1, 1, 1, 1};
     dims[0] = static_cast<cuuint64_t>(head_dim);
-    box[0] = pd::kBoxCols;
+    box[0] = static_cast<cuuint32_t>(box_cols);
     if (tok_first) {
         dims[1] = block_size;
-        strides[0] = static_cast<cuuint64_t>(tok_stride) * 2;
+        strides[0] = static_cast<cuuint64_t>(tok_stride) * elem;
         box[1] = pd::kTileTokens;
         dims[2] = num_kv_heads;
-        strides[1] = static_cast<cuuint64_t>(kvh_stride) * 2;
+        strides[1] = static_cast<cuuint64_t>(kvh_stride) * elem;
         box[2] = 1;
     } else {
         dims[1] = num_kv_heads;
-        strides[0] = static_cast<cuuint64_t>(kvh_stride) * 2;
+        strides[0] = static_cast<cuuint64_t>(kvh_stride) * elem;
         box[1] = 1;
         dims[2] = block_size;
-        strides[1] = static_cast<cuuint64_t>(tok_stride) * 2;
+        strides[1] = static_cast<cuuint64_t>(tok_stride) * elem;
         box[2] = pd::kTileTokens;
     }
     dims[3] = static_cast<cuuint64_t>(num_blocks);
-    strides[2] = static_cast<cuuint64_t>(blk_stride) * 2;
+    strides[2] = static_cast<cuuint64_t>(blk_stride) * elem;
     box[3] = 1;
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(map, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     elem == 1 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PD_ERR_INVALID,
@@ -228,13 +235,15 @@ int g_debug_stages = 0;
 int g_debug_cluster = 0;
 int g_debug_lpt = -1;
 
-int default_stages(int dpad) {
+int default_stages(int dpad, bool kv8 = false) {
     if (g_debug_stages > 0) return g_debug_stages;
+    if (kv8) return dpad <= 128 ? 2 : 1;  // an FP8 tile is half a BF16 one
     return dpad <= 64 ? 2 : 1;
 }
 
-int default_stages_seq(int dpad) {
+int default_stages_seq(int dpad, bool kv8 = false) {
     if (g_debug_stages > 0) return g_debug_stages;
+    if (kv8) return dpad <= 128 ? 4 : 2;
     return dpad <= 128 ? 2 : 1;
 }
 
@@ -256,18 +265,21 @@ int max_parts_for(int dpad, bool tiled) { return tiled ? 2 : (dpad >= 256 ? 8 : 
 
 int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
 
-template <int MODE>
+template <int MODE, bool KV8>
 cudaError_t dispatch_unit(int dpad, int gn, bool hl, bool packed, const CUtensorMap &tk,
                           const CUtensorMap &tv, const pd::UnitParams &p, long long units,
                           int stages_seq, cudaStream_t st) {
     using namespace pd;
     const int layout = g_debug_cluster == 1 ? 1 : (g_debug_cluster > 1 ? 2 : 0);
-    if (packed) return launch_unit<256, 1, false, kModePaged, true>(tk, tv, p, units, stages_seq, st, layout);
-#define PD_DISPATCH_D(DP)                                                                          \
-    if (dpad == DP) {                                                                              \
-        if (gn == 2) return launch_unit<DP, 2, false, MODE, false>(tk, tv, p, units, stages_seq, st, layout); \
-        if (hl) return launch_unit<DP, 1, true, MODE, false>(tk, tv, p, units, stages_seq, st, layout);       \
-        return launch_unit<DP, 1, false, MODE, false>(tk, tv, p, units, stages_seq, st, layout);              \
+    if constexpr (MODE == kModePaged) {
+        if (packed)
+            return launch_unit<256, 1, false, kModePaged, true, KV8>(tk, tv, p, units, stages_seq, st, layout);
+    }
+#define PD_DISPATCH_D(DP)                                                                              \
+    if (dpad == DP) {                                                                                  \
+        if (gn == 2) return launch_unit<DP, 2, false, MODE, false, KV8>(tk, tv, p, units, stages_seq, st, layout); \
+        if (hl) return launch_unit<DP, 1, true, MODE, false, KV8>(tk, tv, p, units, stages_seq, st, layout);       \
+        return launch_unit<DP, 1, false, MODE, false, KV8>(tk, tv, p, units, stages_seq, st, layout);              \
     }
     PD_DISPATCH_D(64)
     PD_DISPATCH_D(128)
@@ -469,12 +481,15 @@ int pd_split_chunk_tokens(int context_len, int num_splits, int block_size) {
 
 // ---- paged decode ----------------------------------------------------------------------
 
-int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
-                   const int32_t *block_table, int max_blocks_per_seq,
-                   const int32_t *context_lens, void *out, int num_seqs, int num_q_heads,
-                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                   float inv_sqrt_d, int num_splits, void *workspace, size_t workspace_bytes,
-                   int gqa_pack, void *stream) {
+namespace {
+// pd_decode_attn over a BF16 cache (kv8 false) or an FP8 E4M3 cache with
+// per-tensor scales (kv8 true); one body so that both take the same checks,
+// split geometry, launch choices and merge.
+int decode_impl(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                int max_blocks_per_seq, const int32_t *context_lens, void *out, int num_seqs,
+                int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                float inv_sqrt_d, int num_splits, void *workspace, size_t workspace_bytes, int gqa_pack,
+                void *stream, bool kv8, float k_scale, float v_scale) {
     if (gqa_pack < PD_GQA_PACK_OFF || gqa_pack > PD_GQA_PACK_SPLITK)
         return fail(PD_ERR_INVALID, "gqa_pack must be 0, 1 or 2");
     if (gqa_pack) {
@@ -489,6 +504,12 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     }
     int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size);
     if (rc != PD_OK) return rc;
+    if (kv8) {
+        if (head_dim % 16 != 0)
+            return fail(PD_ERR_UNSUPPORTED, "FP8 cache: head_dim %d must be a multiple of 16", head_dim);
+        if (!std::isfinite(k_scale) || !std::isfinite(v_scale))
+            return fail(PD_ERR_INVALID, "FP8 cache: k_scale and v_scale must be finite");
+    }
     if (num_seqs < 0) return fail(PD_ERR_INVALID, "num_seqs %d < 0", num_seqs);
     if (num_splits < 1 || num_splits > 4096)
         return fail(PD_ERR_INVALID, "num_splits %d outside 1..4096", num_splits);
@@ -517,7 +538,7 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     const int gn = packed ? 1 : (G <= 8 ? 1 : 2);
     const int rows = 8 * gn;
     const int qtiles = (G + rows - 1) / rows;
-    const int stages = default_stages(dpad);
+    const int stages = default_stages(dpad, kv8);
     const long long units = static_cast<long long>(num_seqs) * num_kv_heads * qtiles * num_splits;
     if (units * max_parts_for(dpad, false) > 0x7fffffffLL)
         return fail(PD_ERR_INVALID, "launch too large (%lld units)", units);
@@ -530,11 +551,13 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     int tok_dim = 1;
     const long long kvh_s = head_dim, tok_s = static_cast<long long>(num_kv_heads) * head_dim;
     const long long blk_s = tok_s * block_size;
+    const int elem = kv8 ? 1 : 2;
+    const int box_cols = kv8 ? dpad : pd::kBoxCols;
     rc = encode_kv_map(&tk, &tok_dim, k_cache, head_dim, block_size, num_kv_heads, num_blocks, blk_s,
-                       tok_s, kvh_s);
+                       tok_s, kvh_s, elem, box_cols);
     if (rc != PD_OK) return rc;
     rc = encode_kv_map(&tv, &tok_dim, v_cache, head_dim, block_size, num_kv_heads, num_blocks, blk_s,
-                       tok_s, kvh_s);
+                       tok_s, kvh_s, elem, box_cols);
     if (rc != PD_OK) return rc;
 
     pd::UnitParams p = {};
@@ -562,20 +585,24 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
     p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = default_lpt(num_seqs);
-    p.prefetch_tiles = kPrefetchBytes / (64 * dpad);
+    p.prefetch_tiles = kPrefetchBytes / (2 * pd::kTileTokens * dpad * elem);
     p.tok_dim = tok_dim;
-    p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
+    // An FP8 cache's K scale multiplies every score: fold it into the softmax scale.
+    p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * (kv8 ? static_cast<double>(k_scale) : 1.0) *
+                                      1.4426950408889634);
+    p.v_scale = kv8 ? v_scale : 1.f;
     p.status = status;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int smem = pd::unit_smem_bytes(dpad, rows, stages);
+    const int smem = pd::unit_smem_bytes(dpad, rows, stages, kv8);
     if (smem > max_smem_optin())
         return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
                     smem, max_smem_optin());
-    int stages_seq = default_stages_seq(dpad);
-    if (pd::unit_smem_bytes(dpad, rows, stages_seq) > max_smem_optin()) stages_seq = stages;
-    cudaError_t e = dispatch_unit<pd::kModePaged>(dpad, gn, !packed && G <= 4, packed, tk, tv, p, units,
-                                                  stages_seq, st);
+    int stages_seq = default_stages_seq(dpad, kv8);
+    if (pd::unit_smem_bytes(dpad, rows, stages_seq, kv8) > max_smem_optin()) stages_seq = stages;
+    const bool hl = !packed && G <= 4;
+    cudaError_t e = kv8 ? dispatch_unit<pd::kModePaged, true>(dpad, gn, hl, packed, tk, tv, p, units, stages_seq, st)
+                        : dispatch_unit<pd::kModePaged, false>(dpad, gn, hl, packed, tk, tv, p, units, stages_seq, st);
     if (e != cudaSuccess) return cuda_fail(e, "unit kernel launch");
     if (num_splits > 1) {
         pd::MergeParams mp = {};
@@ -594,6 +621,28 @@ int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
     }
     return ok();
+}
+}  // namespace
+
+int pd_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                   const int32_t *block_table, int max_blocks_per_seq,
+                   const int32_t *context_lens, void *out, int num_seqs, int num_q_heads,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   float inv_sqrt_d, int num_splits, void *workspace, size_t workspace_bytes,
+                   int gqa_pack, void *stream) {
+    return decode_impl(q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, out, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, inv_sqrt_d, num_splits,
+                       workspace, workspace_bytes, gqa_pack, stream, false, 1.f, 1.f);
+}
+
+int pd_decode_attn_fp8(const void *q, const void *k_cache, const void *v_cache, float k_scale,
+                       float v_scale, const int32_t *block_table, int max_blocks_per_seq,
+                       const int32_t *context_lens, void *out, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks, float inv_sqrt_d,
+                       int num_splits, void *workspace, size_t workspace_bytes, int gqa_pack, void *stream) {
+    return decode_impl(q, k_cache, v_cache, block_table, max_blocks_per_seq, context_lens, out, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, inv_sqrt_d, num_splits,
+                       workspace, workspace_bytes, gqa_pack, stream, true, k_scale, v_scale);
 }
 
 // ---- tiled ----------------------------------------------------------------------------------
@@ -807,14 +856,14 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     const float inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.head_dim)));
     p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
     p.status = status;
-    const int smem = pd::unit_smem_bytes(dpad, rows, stages);
+    const int smem = pd::unit_smem_bytes(dpad, rows, stages, false);
     if (smem > max_smem_optin())
         return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
                     smem, max_smem_optin());
     int stages_seq = default_stages_seq(dpad);
-    if (pd::unit_smem_bytes(dpad, rows, stages_seq) > max_smem_optin()) stages_seq = stages;
-    cudaError_t e = dispatch_unit<pd::kModeTiled>(dpad, gn, G <= 4, false, tk, tv, p, units, stages_seq,
-                                                  static_cast<cudaStream_t>(stream));
+    if (pd::unit_smem_bytes(dpad, rows, stages_seq, false) > max_smem_optin()) stages_seq = stages;
+    cudaError_t e = dispatch_unit<pd::kModeTiled, false>(dpad, gn, G <= 4, false, tk, tv, p, units, stages_seq,
+                                                         static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tiled step launch");
     return ok();
 }

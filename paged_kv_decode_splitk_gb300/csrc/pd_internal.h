@@ -72,7 +72,8 @@ struct UnitParams {
     int lpt;          // paged mode: serve sequences longest first (needs num_seqs <= kLptMaxSeqs)
     int prefetch_tiles;  // first tiles of the CTA's part prefetched into L2 before the wait (0: none)
     int tok_dim;      // tensor-map dimension of the token coordinate (1 or 2)
-    float scale_log2; // softmax scale * log2(e)
+    float scale_log2; // softmax scale * log2(e) (times k_scale for an FP8 cache)
+    float v_scale;    // FP8 cache: V = code value * v_scale (unused for BF16)
     unsigned int *status;  // device status word (PD_DEV_* flags)
 };
 
@@ -88,14 +89,14 @@ struct MergeParams {
 // Record an error message for pd_last_error() and return `code`.
 int report_error(int code, const char *message);
 
-// Dynamic shared memory a unit CTA needs.
-int unit_smem_bytes(int dpad, int rows, int stages);
+// Dynamic shared memory a unit CTA needs (kv8: FP8 cache).
+int unit_smem_bytes(int dpad, int rows, int stages, bool kv8);
 
 // Kernel launchers (defined in the per-head-dim translation units).
 // layout: 0 = choose from occupancy, 1 = one CTA per unit, 2 = one CTA per part.
 // p.stages is the ring depth per warp of a single-wave launch, stages_seq that
 // of a launch of several waves of one-CTA units (both must fit the device).
-template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
+template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8>
 cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p,
                         long long units, int stages_seq, cudaStream_t stream, int layout);
 

@@ -76,6 +76,7 @@ __device__ __forceinline__ float fold_value(float r, float a, float pv, float b)
 // reuse the stage ring once every tile has been consumed.
 struct UnitSmem {
     int stages;  // stage ring (offset 0, 1024-aligned)
+    int cvt;     // FP8 caches: one BF16 tile per warp, converted from the landed FP8 tile
     int merge;   // per-warp o [kWarps][rows][dpad+4]: overlaps the ring
     int result;  // CTA result o [rows][dpad+4], read by the cluster peers: overlaps the ring
     int qs;      // the CTA's query rows, BF16, padded rows
@@ -89,18 +90,22 @@ __host__ __device__ constexpr int unit_stat_floats(int rows) {
     return rows * (3 * kWarps + 2 + 4 + 2 * kMaxParts + 2);
 }
 
-__host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stages_per_warp) {
+__host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stages_per_warp,
+                                                   bool kv8 = false) {
     UnitSmem s;
-    const int stage_bytes = 2 * kTileTokens * dpad * 2;
+    const int elem = kv8 ? 1 : 2;
+    const int stage_bytes = 2 * kTileTokens * dpad * elem;
     const int ring = kWarps * stages_per_warp * stage_bytes;
     const int ostride = dpad + 4;
     const int merge = kWarps * rows * ostride * 4;
     const int result = rows * ostride * 4;
     s.stages = 0;
+    s.cvt = (ring + 1023) / 1024 * 1024;
+    const int loop_end = kv8 ? s.cvt + kWarps * kTileTokens * dpad * 2 : ring;
     s.merge = 0;
     s.result = merge;
     int end = s.result + result;
-    if (ring > end) end = ring;
+    if (loop_end > end) end = loop_end;
     s.qs = (end + 15) / 16 * 16;
     s.stats = s.qs + rows * (dpad * 2 + 16);
     s.bars = s.stats + (unit_stat_floats(rows) * 4 + 15) / 16 * 16;
@@ -109,14 +114,51 @@ __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stage
     return s;
 }
 
-template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
+// FP8 E4M3 tile (16 rows x DPAD bytes, row-major, as the TMA landed it) ->
+// f16 tile in the 128-byte-swizzled box layout the BF16 path loads, so the same
+// ldmatrix addressing serves both.  One hardware conversion per code pair;
+// every E4M3 value (subnormals included) is an f16 value, so it is exact.  The
+// products of an FP8 cache then run on the f16 tensor-core path.
+template <int DPAD>
+__device__ __forceinline__ void e4m3_tile_to_f16(const uint8_t *src, uint8_t *dst, int lane) {
+    constexpr int CPR = DPAD / 16;  // 16-byte chunks per FP8 row
+#pragma unroll 2
+    for (int i = 0; i < DPAD / 32; ++i) {
+        const int c = lane + 32 * i;
+        const int t = c / CPR, k = c - t * CPR;
+        const uint4 v = *reinterpret_cast<const uint4 *>(src + c * 16);
+        uint4 lo, hi;
+        dev::e4m3x4_to_f16x4(v.x, lo.x, lo.y);
+        dev::e4m3x4_to_f16x4(v.y, lo.z, lo.w);
+        dev::e4m3x4_to_f16x4(v.z, hi.x, hi.y);
+        dev::e4m3x4_to_f16x4(v.w, hi.z, hi.w);
+        const int col = 16 * k;
+        uint8_t *box = dst + (col / kBoxCols) * (kTileTokens * 128);
+        const int c8 = (col % kBoxCols) / 8;
+        *reinterpret_cast<uint4 *>(box + t * 128 + ((c8 ^ (t & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(box + t * 128 + (((c8 + 1) ^ (t & 7)) << 4)) = hi;
+    }
+}
+
+// The tensor-core product of the path: BF16 operands, or f16 over an FP8 cache.
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    if constexpr (F16)
+        dev::mma_f16_16816(d, a0, a1, a2, a3, b0, b1);
+    else
+        dev::mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
+}
+
+template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8>
 __global__ void __launch_bounds__(kThreads)
     unit_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const __grid_constant__ UnitParams p) {
     constexpr int KS = DPAD / 16;      // mma k-steps of K.q^T == m-tiles of V^T.P^T
-    constexpr int NBOX = DPAD / kBoxCols;
-    constexpr int TILE_BYTES = kTileTokens * DPAD * 2;
+    constexpr int NBOX = DPAD / kBoxCols;                 // BF16 boxes per tile (64 columns each)
+    constexpr int TILE_BYTES = kTileTokens * DPAD * (KV8 ? 1 : 2);  // one landed K or V tile
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static_assert(!KV8 || MODE == kModePaged, "FP8 caches are a paged-mode source");
     constexpr int RT = 8 * GN;         // query rows per CTA
     constexpr int OSTRIDE = DPAD + 4;  // padded row stride of o in shared memory
     constexpr int QST = DPAD * 2 + 16; // padded row stride of q in shared memory (bytes)
@@ -128,7 +170,7 @@ __global__ void __launch_bounds__(kThreads)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int S = p.stages;
-    const UnitSmem plan = unit_smem_plan(DPAD, RT, S);
+    const UnitSmem plan = unit_smem_plan(DPAD, RT, S, KV8);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + plan.bars);  // [kWarps*S][K, V]
     // Cluster hand-off (one phase each): `ready` of a row owner completes when
     // every active rank has published its part; `done` of an active rank when
@@ -244,7 +286,7 @@ __global__ void __launch_bounds__(kThreads)
                         const int c1 = p.tok_dim == 1 ? sub : kvh;
                         const int c2 = p.tok_dim == 1 ? kvh : sub;
 #pragma unroll
-                        for (int b = 0; b < NBOX; ++b) {
+                        for (int b = 0; b < (KV8 ? 1 : NBOX); ++b) {
                             dev::tma_prefetch_4d(&tmk, b * kBoxCols, c1, c2, id);
                             dev::tma_prefetch_4d(&tmv, b * kBoxCols, c1, c2, id);
                         }
@@ -333,12 +375,43 @@ __global__ void __launch_bounds__(kThreads)
     if (C > 1 && part >= V) return;
 
     // ---- q to shared memory (the barriers were initialised at the start) ----------
+    // Over an FP8 cache the products run in f16: q is staged as f16 scaled by a
+    // power of two 2^-kq that brings the CTA's largest |q| below 2^15 (kq = 0
+    // for ordinary q, where the conversion is exact), and 2^kq goes back into
+    // the softmax scale.  The rows are one (sequence, KV head)'s, so kq depends
+    // on the sequence's own q only.
+    float scale_log2 = p.scale_log2;
+    if constexpr (KV8) {
+        float qmax = 0.f;
 #pragma unroll
-    for (int i = 0; i < QPT; ++i) {
-        const int e = tid + i * kThreads;
-        const int g = e / (DPAD / 2);
-        const int d = (e - g * (DPAD / 2)) * 2;
-        *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) = qv[i];
+        for (int i = 0; i < QPT; ++i)
+            qmax = fmaxf(qmax, fmaxf(fabsf(dev::bf16_lo_f32(qv[i])), fabsf(dev::bf16_hi_f32(qv[i]))));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+        if (lane == 0) stats[warp] = qmax;
+        __syncthreads();
+        qmax = fmaxf(fmaxf(stats[0], stats[1]), fmaxf(stats[2], stats[3]));
+        // qmax < 2^(E - 126) for a normal float with biased exponent E
+        const int ex = ((__float_as_int(qmax) >> 23) & 0xff) - 126;
+        const int kq = ex > 15 ? (ex - 15 < 126 ? ex - 15 : 126) : 0;
+        const float down = __int_as_float((127 - kq) << 23);
+        scale_log2 = p.scale_log2 * __int_as_float((127 + kq) << 23);
+#pragma unroll
+        for (int i = 0; i < QPT; ++i) {
+            const int e = tid + i * kThreads;
+            const int g = e / (DPAD / 2);
+            const int d = (e - g * (DPAD / 2)) * 2;
+            *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) =
+                dev::pack_f16x2(dev::bf16_lo_f32(qv[i]) * down, dev::bf16_hi_f32(qv[i]) * down);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < QPT; ++i) {
+            const int e = tid + i * kThreads;
+            const int g = e / (DPAD / 2);
+            const int d = (e - g * (DPAD / 2)) * 2;
+            *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) = qv[i];
+        }
     }
     // Running result of the parts folded so far (cluster == 1), starting empty:
     // m and l per row in shared memory, o in registers (element e = tid + i *
@@ -413,8 +486,9 @@ __global__ void __launch_bounds__(kThreads)
             const int c1 = p.tok_dim == 1 ? sub : kvh;
             const int c2 = p.tok_dim == 1 ? kvh : sub;
             dev::mbar_arrive_expect_tx(bar, TILE_BYTES);
+            // BF16: NBOX swizzled boxes of 64 columns; FP8: one unswizzled box of the whole row
 #pragma unroll
-            for (int b = 0; b < NBOX; ++b)
+            for (int b = 0; b < (KV8 ? 1 : NBOX); ++b)
                 dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * kBoxCols, c1, c2, id, policy);
         };
 
@@ -479,8 +553,19 @@ __global__ void __launch_bounds__(kThreads)
             }
             const int gt = my0 + warp + kWarps * r;
             const int nvalid = min(kTileTokens, tok1 - gt * kTileTokens);
-            const uint32_t kbase = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES);
-            const uint32_t vbase = kbase + TILE_BYTES;
+            uint8_t *stage = ring + (warp * S + k) * STAGE_BYTES;
+            uint32_t kbase = dev::smem_addr(stage);
+            uint32_t vbase = kbase + TILE_BYTES;
+            uint8_t *cvt = smem + plan.cvt + warp * (kTileTokens * DPAD * 2);
+            if constexpr (KV8) {
+                // K: FP8 stage -> the warp's f16 tile; the stage is then free for tile r + S
+                __syncwarp();  // the previous tile's reads of the f16 tile are done
+                e4m3_tile_to_f16<DPAD>(stage, cvt, lane);
+                __syncwarp();
+                if (rn < nloc && lane == 0) issue(&tmk, 0, rn, k, id_next);
+                kbase = dev::smem_addr(cvt);
+                vbase = kbase;
+            }
 
             // S^T = K . q^T, two accumulator chains (even / odd k-steps)
             float sc[GN][2][4];
@@ -498,15 +583,17 @@ __global__ void __launch_bounds__(kThreads)
                 for (int nt = 0; nt < GN; ++nt) {
                     uint32_t b0, b1;
                     dev::ldsm_x2(q_lm + nt * 8 * QST + ks * 32, b0, b1);
-                    dev::mma_bf16_16816(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
+                    mma_16816<KV8>(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
                 }
             }
             // The K half is read (every lane's ldmatrix result has been consumed by
             // an mma): refill it with tile r + S.  A read-then-overwrite by the TMA
             // needs no proxy fence once the read values are in registers.
-            if (rn < nloc) {
-                __syncwarp();
-                if (lane == 0) issue(&tmk, 0, rn, k, id_next);
+            if constexpr (!KV8) {
+                if (rn < nloc) {
+                    __syncwarp();
+                    if (lane == 0) issue(&tmk, 0, rn, k, id_next);
+                }
             }
 
             // column softmax over the tile's tokens, base 2, tokens past the range masked
@@ -518,7 +605,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int t = tq + (c >> 1) * 8;
-                    const float v = (sc[nt][0][c] + sc[nt][1][c]) * p.scale_log2;
+                    const float v = (sc[nt][0][c] + sc[nt][1][c]) * scale_log2;
                     x[c] = t < nvalid ? v : kNegInf;
                 }
                 float cmx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
@@ -548,8 +635,14 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const float e0 = pv[nt][2 * h2], e1 = pv[nt][2 * h2 + 1];
-                    const uint32_t hi = dev::pack_bf16x2(e0, e1);
-                    const uint32_t lo = dev::pack_bf16x2(e0 - dev::bf16_lo_f32(hi), e1 - dev::bf16_hi_f32(hi));
+                    uint32_t hi, lo;
+                    if constexpr (KV8) {
+                        hi = dev::pack_f16x2(e0, e1);
+                        lo = dev::pack_f16x2(e0 - dev::f16_lo_f32(hi), e1 - dev::f16_hi_f32(hi));
+                    } else {
+                        hi = dev::pack_bf16x2(e0, e1);
+                        lo = dev::pack_bf16x2(e0 - dev::bf16_lo_f32(hi), e1 - dev::bf16_hi_f32(hi));
+                    }
                     bh[nt][h2] = dev::movmatrix_trans(hi);
                     bl[nt][h2] = dev::movmatrix_trans(lo);
                 }
@@ -593,6 +686,13 @@ __global__ void __launch_bounds__(kThreads)
                 fail_r = r;
                 break;
             }
+            if constexpr (KV8) {
+                // V: FP8 stage -> the same f16 tile (q.K^T has read it)
+                __syncwarp();
+                e4m3_tile_to_f16<DPAD>(stage + TILE_BYTES, cvt, lane);
+                __syncwarp();
+                if (rn < nloc && lane == 0) issue(&tmv, 1, rn, k, id_next);
+            }
             // O^T += V^T . P^T  (V rows past the range may hold anything: mask them)
             auto pv_tile = [&](uint32_t mask01, uint32_t mask89) {
 #pragma unroll
@@ -605,8 +705,8 @@ __global__ void __launch_bounds__(kThreads)
                     a3 &= mask89;
 #pragma unroll
                     for (int nt = 0; nt < GN; ++nt) {
-                        dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                        if constexpr (!HL) dev::mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                        mma_16816<KV8>(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                        if constexpr (!HL) mma_16816<KV8>(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
                     }
                 }
             };
@@ -618,9 +718,11 @@ __global__ void __launch_bounds__(kThreads)
                         (tv0 + 8 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 9 < nvalid ? 0xffff0000u : 0u));
             }
             // the V half is read: refill it with tile r + S
-            if (rn < nloc) {
-                __syncwarp();
-                if (lane == 0) issue(&tmv, 1, rn, k, id_next);
+            if constexpr (!KV8) {
+                if (rn < nloc) {
+                    __syncwarp();
+                    if (lane == 0) issue(&tmv, 1, rn, k, id_next);
+                }
             }
         }
         if (fail_r >= 0) {
@@ -846,6 +948,10 @@ __global__ void __launch_bounds__(kThreads)
             acc1 = co[g * OSTRIDE + d + 1];
         }
         const long long row = static_cast<long long>(s) * Hq + h0 + g;
+        if constexpr (KV8) {  // V = code value * v_scale
+            acc0 *= p.v_scale;
+            acc1 *= p.v_scale;
+        }
         if constexpr (MODE == kModePaged) {
             if (direct) {
                 const float Lsum = fx[i * 4 + 1];

@@ -8,12 +8,10 @@
 
 namespace pd {
 
-int unit_smem_bytes(int dpad, int rows, int stages);
-
-template <int DPAD, int GN, bool HL, int MODE, bool PACKED>
+template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8>
 cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p_in,
                         long long units, int stages_seq, cudaStream_t stream, int layout) {
-    auto kern = unit_kernel<DPAD, GN, HL, MODE, PACKED>;
+    auto kern = unit_kernel<DPAD, GN, HL, MODE, PACKED, KV8>;
     // Per device: the dynamic shared-memory limit raised so far, the SM count,
     // and how many CTAs of this kernel fit on one SM at each stage count.
     static std::mutex mu;
@@ -27,7 +25,7 @@ cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const Un
     if (p_in.stages < 1 || p_in.stages > kMaxStagesPerWarp || stages_seq < 1 || stages_seq > kMaxStagesPerWarp)
         return cudaErrorInvalidValue;
     auto slots_for = [&](int stages, int *smem_out) -> cudaError_t {
-        const int smem = unit_smem_plan(DPAD, 8 * GN, stages).total;
+        const int smem = unit_smem_plan(DPAD, 8 * GN, stages, KV8).total;
         *smem_out = smem;
         std::lock_guard<std::mutex> lock(mu);
         if (configured[dev] < smem) {
@@ -105,7 +103,7 @@ cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const Un
 
 }  // namespace pd
 
-#define PD_INSTANTIATE_UNIT(DPAD, GN, HL, MODE, PACKED)                                      \
-    template cudaError_t pd::launch_unit<DPAD, GN, HL, MODE, PACKED>(                        \
+#define PD_INSTANTIATE_UNIT(DPAD, GN, HL, MODE, PACKED, KV8)                                 \
+    template cudaError_t pd::launch_unit<DPAD, GN, HL, MODE, PACKED, KV8>(                   \
         const CUtensorMap &, const CUtensorMap &, const pd::UnitParams &, long long, int,       \
         cudaStream_t, int);

@@ -94,6 +94,8 @@ _SIGS = {
     "pd_split_chunk_tokens": (_I, [_I, _I, _I]),
     "pd_decode_attn": (_I, [_VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I,
                             ctypes.c_float, _I, _VP, _SZ, _I, _VP]),
+    "pd_decode_attn_fp8": (_I, [_VP, _VP, _VP, ctypes.c_float, ctypes.c_float, _VP, _I, _VP, _VP, _I, _I,
+                                _I, _I, _I, _I, ctypes.c_float, _I, _VP, _SZ, _I, _VP]),
     "pd_decode_attn_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _I, _I,
                                     ctypes.c_float, _I, _I, _VP]),
     "pd_tiled_validate": (_I, [_VP]),
@@ -256,6 +258,24 @@ def pd_decode_attn(q, k_cache, v_cache, block_table, context_lens, out, inv_sqrt
                               D, bs, nb if num_blocks is None else num_blocks, float(inv_sqrt_d),
                               int(num_splits), _ptr(workspace), ws_bytes, int(gqa_pack),
                               _stream(stream))
+    return _check(rc)
+
+
+def pd_decode_attn_fp8(q, k_cache, v_cache, k_scale: float, v_scale: float, block_table, context_lens,
+                       out, inv_sqrt_d: float, num_splits: int, workspace=None, gqa_pack: int = 0,
+                       stream=None, num_blocks: int | None = None) -> int:
+    """pd_decode_attn over an FP8 E4M3 cache: k_cache / v_cache uint8 tensors
+    [num_blocks, block_size, Hkv, D] of E4M3 codes, K = value * k_scale, V = value * v_scale."""
+    S, Hq, D = q.shape
+    nb, bs, Hkv, D2 = k_cache.shape
+    assert D2 == D, "head_dim mismatch"
+    assert k_cache.element_size() == 1 and v_cache.element_size() == 1, "FP8 caches are 1-byte codes"
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().pd_decode_attn_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale), float(v_scale),
+                                  _ptr(block_table), int(block_table.shape[1]), _ptr(context_lens), _ptr(out),
+                                  S, Hq, Hkv, D, bs, nb if num_blocks is None else num_blocks,
+                                  float(inv_sqrt_d), int(num_splits), _ptr(workspace), ws_bytes,
+                                  int(gqa_pack), _stream(stream))
     return _check(rc)
 
 

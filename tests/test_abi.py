@@ -206,12 +206,37 @@ def _call(L, **kw):
     (dict(N=2, ws=16, wsb=100), pd.PD_ERR_WORKSPACE),
     (dict(pack=1), pd.PD_NOT_APPLICABLE),       # 8/2 heads at D=128: not the packed shape
     (dict(pack=1, Hq=16, Hkv=2, D=256, N=2), pd.PD_NOT_APPLICABLE),
-    (dict(pack=2), pd.PD_ERR_INVALID),
+    (dict(pack=2), pd.PD_NOT_APPLICABLE),       # the split-K packed mode keeps the shape gate
+    (dict(pack=3), pd.PD_ERR_INVALID),
+    (dict(pack=-1), pd.PD_ERR_INVALID),
 ])
 def test_decode_attn_rejects(L, kw, code):
     assert _call(L, **kw) == code
     if code != pd.PD_OK:
         assert pd.last_error() != ""
+
+
+def _call_fp8(L, ks=1.0, vs=1.0, **kw):
+    a = dict(q=16, k=16, v=16, bt=16, maxb=4, cl=16, out=16, S=1, Hq=8, Hkv=2, D=128, bs=16, nb=8,
+             scale=0.1, N=1, ws=None, wsb=0, pack=0)
+    a.update(kw)
+    P_ = ctypes.c_void_p
+    return L.pd_decode_attn_fp8(P_(a["q"]), P_(a["k"]), P_(a["v"]), ks, vs, P_(a["bt"]), a["maxb"],
+                                P_(a["cl"]), P_(a["out"]), a["S"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["nb"],
+                                a["scale"], a["N"], P_(a["ws"]) if a["ws"] else None, a["wsb"], a["pack"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=40), pd.PD_ERR_UNSUPPORTED),        # an FP8 row must be a whole number of 16-byte chunks
+    (dict(ks=float("inf")), pd.PD_ERR_INVALID),
+    (dict(vs=float("nan")), pd.PD_ERR_INVALID),
+    (dict(Hq=6, Hkv=4), pd.PD_ERR_INVALID),
+    (dict(N=2), pd.PD_ERR_WORKSPACE),
+    (dict(pack=1), pd.PD_NOT_APPLICABLE),
+])
+def test_decode_attn_fp8_rejects(L, kw, code):
+    assert _call_fp8(L, **kw) == code
+    assert pd.last_error() != ""
 
 
 def test_zero_sequences_is_a_no_op(L):
