@@ -62,10 +62,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // Arrive `count` (>= 1) times on a barrier of this CTA.
 __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) {
-    uint64_t state;
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 %0, [%1], %2;"
-                 : "=l"(state)
-                 : "r"(bar), "r"(count)
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count)
                  : "memory");
 }
 

@@ -76,7 +76,7 @@ __device__ __forceinline__ float fold_value(float r, float a, float pv, float b)
 // reuse the stage ring once every tile has been consumed.
 struct UnitSmem {
     int stages;  // stage ring (offset 0, 1024-aligned)
-    int cvt;     // FP8 caches: one BF16 tile per warp, converted from the landed FP8 tile
+    int cvt;     // FP8 caches: the f16 tiles each warp converts the landed FP8 tiles into
     int merge;   // per-warp o [kWarps][rows][dpad+4]: overlaps the ring
     int result;  // CTA result o [rows][dpad+4], read by the cluster peers: overlaps the ring
     int qs;      // the CTA's query rows, BF16, padded rows
@@ -101,7 +101,8 @@ __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stage
     const int result = rows * ostride * 4;
     s.stages = 0;
     s.cvt = (ring + 1023) / 1024 * 1024;
-    const int loop_end = kv8 ? s.cvt + kWarps * kTileTokens * dpad * 2 : ring;
+    const int cvt_tiles = dpad <= 128 ? 2 : 1;  // K and V apart, or one tile shared in turn
+    const int loop_end = kv8 ? s.cvt + kWarps * cvt_tiles * kTileTokens * dpad * 2 : ring;
     s.merge = 0;
     s.result = merge;
     int end = s.result + result;
@@ -122,7 +123,9 @@ __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stage
 template <int DPAD>
 __device__ __forceinline__ void e4m3_tile_to_f16(const uint8_t *src, uint8_t *dst, int lane) {
     constexpr int CPR = DPAD / 16;  // 16-byte chunks per FP8 row
-#pragma unroll 2
+    // every chunk in flight at head dims up to 128; two at a time at 256, where
+    // a full unroll would hold every chunk's registers on top of the o accumulators
+#pragma unroll(DPAD <= 128 ? DPAD / 32 : 2)
     for (int i = 0; i < DPAD / 32; ++i) {
         const int c = lane + 32 * i;
         const int t = c / CPR, k = c - t * CPR;
@@ -556,8 +559,26 @@ __global__ void __launch_bounds__(kThreads)
             uint8_t *stage = ring + (warp * S + k) * STAGE_BYTES;
             uint32_t kbase = dev::smem_addr(stage);
             uint32_t vbase = kbase + TILE_BYTES;
-            uint8_t *cvt = smem + plan.cvt + warp * (kTileTokens * DPAD * 2);
-            if constexpr (KV8) {
+            constexpr bool KV8_APART = KV8 && DPAD <= 128;  // K and V in f16 tiles of their own
+            uint8_t *cvt = smem + plan.cvt + warp * (KV8_APART ? 2 : 1) * (kTileTokens * DPAD * 2);
+            if constexpr (KV8_APART) {
+                // both halves landed -> both f16 tiles, converted back to back; the
+                // stage is then free for tile r + S
+                if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 1]), par)) {
+                    fail_r = r;
+                    break;
+                }
+                __syncwarp();  // the previous tile's reads of the f16 tiles are done
+                e4m3_tile_to_f16<DPAD>(stage, cvt, lane);
+                e4m3_tile_to_f16<DPAD>(stage + TILE_BYTES, cvt + kTileTokens * DPAD * 2, lane);
+                __syncwarp();
+                if (rn < nloc && lane == 0) {
+                    issue(&tmk, 0, rn, k, id_next);
+                    issue(&tmv, 1, rn, k, id_next);
+                }
+                kbase = dev::smem_addr(cvt);
+                vbase = kbase + kTileTokens * DPAD * 2;
+            } else if constexpr (KV8) {
                 // K: FP8 stage -> the warp's f16 tile; the stage is then free for tile r + S
                 __syncwarp();  // the previous tile's reads of the f16 tile are done
                 e4m3_tile_to_f16<DPAD>(stage, cvt, lane);
@@ -682,11 +703,13 @@ __global__ void __launch_bounds__(kThreads)
                 }
             }
 
-            if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 1]), par)) {
-                fail_r = r;
-                break;
+            if constexpr (!KV8_APART) {
+                if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 1]), par)) {
+                    fail_r = r;
+                    break;
+                }
             }
-            if constexpr (KV8) {
+            if constexpr (KV8 && !KV8_APART) {
                 // V: FP8 stage -> the same f16 tile (q.K^T has read it)
                 __syncwarp();
                 e4m3_tile_to_f16<DPAD>(stage + TILE_BYTES, cvt, lane);
