@@ -110,6 +110,24 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of the ranks' values (every rank gets it); the identity when
+    the job runs alone."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(kv_bytes_per_rank: int, steps: int, total_ms: float, world_size: int) -> float:
+    """Whole-job KV GB/s: every rank's bytes over the slowest rank's time (the
+    ranks run independent replicas of the same step)."""
+    return world_size * kv_bytes_per_rank * steps / (total_ms / 1e3) / 1e9
+
+
 def _traffic_from_profiles(kernel_tag: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
     kernel source as it is now (the summary records a hash of the sources)."""
@@ -269,13 +287,9 @@ def run_ours(args):
         wall = time.perf_counter() - t0
     if ws > 1:
         dist.barrier()
-    total_ms = evs[0].elapsed_time(evs[-1])
-    t_max = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    total_ms = float(t_max.item())
+    total_ms = max_over_ranks(evs[0].elapsed_time(evs[-1]), dev)
     ms_per_step = total_ms / args.steps
-    value = ws * kv_bytes * args.steps / (total_ms / 1e3) / 1e9
+    value = job_value(kv_bytes, args.steps, total_ms, ws)
     del g_multi, g_single
 
     # dominant kernel: the unit pass (the only launch of a packed / non-split step;
