@@ -210,7 +210,7 @@ def run_ours(args):
                                 t.scratch_pool_strides(), lb))
             srcs.append(lst)
         out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
-        launches_per_step = 2 + len(w.calls)
+        launches_per_step = 2 if len(w.calls) <= 8 else 2 + len(w.calls)
 
         def step(i):
             t.run(base.q, srcs[i % copies], out, w.num_seqs)
@@ -228,13 +228,25 @@ def run_ours(args):
         out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
         launches_per_step = 2 + w.num_calls
 
-        def step(i):
-            p = pools[i % copies].view(-1)
-            t.begin(w.num_seqs)
-            for c in range(w.num_calls):
-                t.step(base.q, p, p[stripe:], base.tile_blocks[c], base.tile_counts[c], w.num_seqs,
-                       strides, int(w.last_block_valid_slots[c]))
-            t.finalize(out, w.num_seqs)
+        # the step through the library's driver, pd_tiled_run (begin, the calls,
+        # finalize in one call; same bits as the calls made one by one), or,
+        # with --tiled-separate, through begin / step_tile x T / finalize
+        srcs = []
+        for i in range(copies):
+            p = pools[i].view(-1)
+            srcs.append([(p, p[stripe:], base.tile_blocks[c], base.tile_counts[c], strides,
+                          int(w.last_block_valid_slots[c])) for c in range(w.num_calls)])
+        if args.tiled_separate:
+            def step(i):
+                t.begin(w.num_seqs)
+                for src in srcs[i % copies]:
+                    t.step(base.q, src[0], src[1], src[2], src[3], w.num_seqs, src[4], src[5])
+                t.finalize(out, w.num_seqs)
+        else:
+            launches_per_step = 2
+
+            def step(i):
+                t.run(base.q, srcs[i % copies], out, w.num_seqs)
         l2_note = f"rotating {copies} scratch-pool copies ({copies * pool_bytes / 1e6:.0f} MB > 129 MB L2)"
 
     warmup = max(3, args.warmup)
@@ -542,6 +554,8 @@ def main():
                              "tiled_mixed", "gqa_packed_fp8", "long_context_fp8", "large_batch_fp8"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tiled-separate", action="store_true",
+                    help="tiled workload: time begin / step_tile x T / finalize as separate calls")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

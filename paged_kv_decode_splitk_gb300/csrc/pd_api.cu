@@ -266,8 +266,8 @@ int max_parts_for(int dpad, bool tiled) { return tiled ? 2 : (dpad >= 256 ? 8 : 
 int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
 
 template <int MODE, bool KV8>
-cudaError_t dispatch_unit(int dpad, int gn, bool hl, bool packed, const CUtensorMap &tk,
-                          const CUtensorMap &tv, const pd::UnitParams &p, long long units,
+cudaError_t dispatch_unit(int dpad, int gn, bool hl, bool packed, const CUtensorMap *tk,
+                          const CUtensorMap *tv, const pd::UnitParams &p, long long units,
                           int stages_seq, cudaStream_t st) {
     using namespace pd;
     const int layout = g_debug_cluster == 1 ? 1 : (g_debug_cluster > 1 ? 2 : 0);
@@ -318,6 +318,7 @@ struct pd_tiled {
     float *l;
     float *o;
     int device;
+    float *run_ws;  // per-call partials of a fused pd_tiled_run, allocated on its first use
 };
 
 namespace {
@@ -601,8 +602,8 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     int stages_seq = default_stages_seq(dpad, kv8);
     if (pd::unit_smem_bytes(dpad, rows, stages_seq, kv8) > max_smem_optin()) stages_seq = stages;
     const bool hl = !packed && G <= 4;
-    cudaError_t e = kv8 ? dispatch_unit<pd::kModePaged, true>(dpad, gn, hl, packed, tk, tv, p, units, stages_seq, st)
-                        : dispatch_unit<pd::kModePaged, false>(dpad, gn, hl, packed, tk, tv, p, units, stages_seq, st);
+    cudaError_t e = kv8 ? dispatch_unit<pd::kModePaged, true>(dpad, gn, hl, packed, &tk, &tv, p, units, stages_seq, st)
+                        : dispatch_unit<pd::kModePaged, false>(dpad, gn, hl, packed, &tk, &tv, p, units, stages_seq, st);
     if (e != cudaSuccess) return cuda_fail(e, "unit kernel launch");
     if (num_splits > 1) {
         pd::MergeParams mp = {};
@@ -717,6 +718,7 @@ void pd_tiled_destroy(pd_tiled *t) {
     cudaFree(t->m);
     cudaFree(t->l);
     cudaFree(t->o);
+    cudaFree(t->run_ws);
     cudaSetDevice(cur);
     delete t;
 }
@@ -862,7 +864,7 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
                     smem, max_smem_optin());
     int stages_seq = default_stages_seq(dpad);
     if (pd::unit_smem_bytes(dpad, rows, stages_seq, false) > max_smem_optin()) stages_seq = stages;
-    cudaError_t e = dispatch_unit<pd::kModeTiled, false>(dpad, gn, G <= 4, false, tk, tv, p, units, stages_seq,
+    cudaError_t e = dispatch_unit<pd::kModeTiled, false>(dpad, gn, G <= 4, false, &tk, &tv, p, units, stages_seq,
                                                          static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tiled step launch");
     return ok();
@@ -881,6 +883,116 @@ int pd_tiled_finalize(pd_tiled *t, void *out, int num_seqs, void *stream) {
     if (e != cudaSuccess) return cuda_fail(e, "tiled finalize launch");
     return ok();
 }
+
+}  // extern "C"
+
+namespace {
+// pd_tiled_run for 1..kMaxRunSources calls in two launches: the unit pass over
+// every (sequence, KV head, call) writes one partial [o, m, l] per call, and
+// the fold pass replays step_tile's fold of those partials in call order from
+// begin's (-inf, 0, 0), then finalizes.  Same arithmetic, same bits, as the
+// calls made one by one.  The partials live in a buffer of the handle,
+// allocated on the first fused run (kMaxRunSources slots per row).
+int tiled_run_fused(pd_tiled *t, const void *q, const pd_tiled_source *sources, int num_sources, void *out,
+                    int num_seqs, void *stream) {
+    const pd_tiled_dims &d = t->dims;
+    if (!t->run_ws) {
+        const size_t n = static_cast<size_t>(d.max_seqs) * d.num_q_heads * pd::kMaxRunSources *
+                         (static_cast<size_t>(d.head_dim) + 2);
+        int inject = g_fail_allocs.load();
+        while (inject > 0 && !g_fail_allocs.compare_exchange_weak(inject, inject - 1)) {
+        }
+        if (inject > 0) return fail(PD_ERR_ALLOC, "fused tiled run: partials buffer (injected failure)");
+        void *ptr = nullptr;
+        cudaError_t ae = cudaMalloc(&ptr, n * sizeof(float));
+        if (ae != cudaSuccess) {
+            cudaGetLastError();
+            return fail(PD_ERR_ALLOC, "fused tiled run: cannot allocate %zu bytes of partials", n * sizeof(float));
+        }
+        t->run_ws = static_cast<float *>(ptr);
+    }
+    const int G = d.num_q_heads / d.num_kv_heads;
+    const int dpad = dpad_for(d.head_dim);
+    const int gn = G <= 8 ? 1 : 2;
+    const int rows = 8 * gn;
+    const int qtiles = (G + rows - 1) / rows;
+    const int stages = default_stages(dpad);
+    const long long units = static_cast<long long>(num_seqs) * d.num_kv_heads * qtiles * num_sources;
+    if (units * max_parts_for(dpad, true) > 0x7fffffffLL) return fail(PD_ERR_INVALID, "launch too large");
+
+    int err = PD_OK;
+    unsigned int *status = status_ptr(&err);
+    if (!status) return err;
+    CUtensorMap tk[pd::kMaxRunSources], tv[pd::kMaxRunSources];
+    pd::UnitParams p = {};
+    for (int c = 0; c < num_sources; ++c) {
+        const pd_tiled_source &src = sources[c];
+        int tok_dim = 1;
+        int rc = encode_kv_map(&tk[c], &tok_dim, src.k_pool, d.head_dim, d.block_size, d.num_kv_heads,
+                               kTiledBlockExtent, src.blk_stride, src.tok_stride, src.kvh_stride);
+        if (rc != PD_OK) return rc;
+        rc = encode_kv_map(&tv[c], &tok_dim, src.v_pool, d.head_dim, d.block_size, d.num_kv_heads,
+                           kTiledBlockExtent, src.blk_stride, src.tok_stride, src.kvh_stride);
+        if (rc != PD_OK) return rc;
+        p.src_blocks[c] = src.tile_blocks;
+        p.src_counts[c] = src.tile_block_counts;
+        p.src_last_valid[c] = src.last_block_valid_slots;
+        p.src_tok_dim[c] = tok_dim;
+    }
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.num_blocks = static_cast<int>(kTiledBlockExtent);
+    p.tile_capacity = d.tile_capacity;
+    p.num_sources = num_sources;
+    p.num_splits = num_sources;  // partial slots per row
+    p.ws_o = t->run_ws;
+    p.ws_ml = t->run_ws + static_cast<size_t>(num_seqs) * d.num_q_heads * num_sources * d.head_dim;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = d.num_q_heads;
+    p.num_kv_heads = d.num_kv_heads;
+    p.group = G;
+    p.head_dim = d.head_dim;
+    p.block_size = d.block_size;
+    p.qtiles = qtiles;
+    p.cluster = 1;
+    p.max_parts = max_parts_for(dpad, true);
+    p.part_tiles = kPartTiles;
+    p.stages = stages;
+    p.lpt = 0;
+    p.prefetch_tiles = 0;
+    p.tok_dim = p.src_tok_dim[0];
+    const float inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d.head_dim)));
+    p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * 1.4426950408889634);
+    p.v_scale = 1.f;
+    p.status = status;
+    const int smem = pd::unit_smem_bytes(dpad, rows, stages, false);
+    if (smem > max_smem_optin())
+        return fail(PD_ERR_INVALID, "launch shape needs %d bytes of shared memory, the device allows %d",
+                    smem, max_smem_optin());
+    int stages_seq = default_stages_seq(dpad);
+    if (pd::unit_smem_bytes(dpad, rows, stages_seq, false) > max_smem_optin()) stages_seq = stages;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = dispatch_unit<pd::kModeTiledRun, false>(dpad, gn, G <= 4, false, tk, tv, p, units, stages_seq, st);
+    if (e != cudaSuccess) return cuda_fail(e, "fused tiled run: unit launch");
+    pd::RunMergeParams mp = {};
+    mp.ws_o = p.ws_o;
+    mp.ws_ml = p.ws_ml;
+    for (int c = 0; c < num_sources; ++c) mp.src_counts[c] = sources[c].tile_block_counts;
+    mp.st_m = t->m;
+    mp.st_l = t->l;
+    mp.st_o = t->o;
+    mp.out = static_cast<__nv_bfloat16 *>(out);
+    mp.num_seqs = num_seqs;
+    mp.num_q_heads = d.num_q_heads;
+    mp.head_dim = d.head_dim;
+    mp.num_sources = num_sources;
+    mp.tile_capacity = d.tile_capacity;
+    e = pd::launch_tiled_run_merge(mp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "fused tiled run: fold launch");
+    return ok();
+}
+}  // namespace
+
+extern "C" {
 
 int pd_tiled_run(pd_tiled *t, const void *q, const pd_tiled_source *sources, int num_sources,
                  void *out, int num_seqs, void *stream) {
@@ -902,6 +1014,8 @@ int pd_tiled_run(pd_tiled *t, const void *q, const pd_tiled_source *sources, int
             return fail(crc, "%s", msg);
         }
     }
+    if (num_sources >= 1 && num_sources <= pd::kMaxRunSources && num_seqs > 0 && t->dims.tile_capacity > 0)
+        return tiled_run_fused(t, q, sources, num_sources, out, num_seqs, stream);
     int rc = pd_tiled_begin(t, num_seqs, stream);
     if (rc != PD_OK) return rc;
     for (int i = 0; i < num_sources; ++i) {

@@ -251,6 +251,20 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Left fold of two (m, l, o) states in base 2: the running state R and the
+// next part P give M = max(mR, mP), a = 2^(mR - M), b = 2^(mP - M) (0 for an
+// empty side), l = lR*a + lP*b, o = oR*a + oP*b.  Rounding is pinned (no
+// contraction) so that every place that folds computes the same bits.
+__device__ __forceinline__ void fold_factors(float mr, float mp, float &mn, float &a, float &b) {
+    const float kNegInf = -__int_as_float(0x7f800000);
+    mn = fmaxf(mr, mp);
+    a = mr == kNegInf ? 0.f : exp2_approx(mr - mn);
+    b = mp == kNegInf ? 0.f : exp2_approx(mp - mn);
+}
+__device__ __forceinline__ float fold_value(float r, float a, float pv, float b) {
+    return __fadd_rn(__fmul_rn(r, a), __fmul_rn(pv, b));
+}
+
 // ---- status word ----------------------------------------------------------
 __device__ __forceinline__ void flag_status(unsigned int *status, unsigned int bits) {
     if (status) atomicOr(status, bits);

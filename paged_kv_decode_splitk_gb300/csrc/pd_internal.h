@@ -36,8 +36,20 @@ __host__ __device__ inline int splits_used(int context_len, int chunk) {
 }
 
 enum UnitMode : int {
-    kModePaged = 0,  // pd_decode_attn: block_table gather, split ranges, out / workspace
-    kModeTiled = 1,  // pd_tiled_step: tile list, fold into the running state
+    kModePaged = 0,     // pd_decode_attn: block_table gather, split ranges, out / workspace
+    kModeTiled = 1,     // pd_tiled_step: tile list, fold into the running state
+    kModeTiledRun = 2,  // pd_tiled_run: every call's tile list at once, one partial per call
+};
+
+// Sources (step_tile calls) one fused pd_tiled_run launch serves at most.
+constexpr int kMaxRunSources = 8;
+
+// The K and V tensor maps a launch reads: one pair, or one per source of a
+// fused tiled run.  Passed by value as a kernel parameter.
+template <int N>
+struct KvMaps {
+    CUtensorMap k[N];
+    CUtensorMap v[N];
 };
 
 // Everything a unit kernel reads besides the two tensor maps.
@@ -55,6 +67,12 @@ struct UnitParams {
     const int32_t *tile_counts;  // [S]
     int tile_capacity;
     int last_valid;
+    // fused tiled run: per source (step_tile call) c < num_sources
+    int num_sources;
+    const int32_t *src_blocks[kMaxRunSources];  // [S, tile_capacity]
+    const int32_t *src_counts[kMaxRunSources];  // [S]
+    int src_last_valid[kMaxRunSources];
+    int src_tok_dim[kMaxRunSources];
     // outputs
     __nv_bfloat16 *out;  // [S, Hq, D]
     float *ws_o;         // [S, Hq, N, D]   unnormalised o of each split
@@ -96,11 +114,24 @@ int unit_smem_bytes(int dpad, int rows, int stages, bool kv8);
 // layout: 0 = choose from occupancy, 1 = one CTA per unit, 2 = one CTA per part.
 // p.stages is the ring depth per warp of a single-wave launch, stages_seq that
 // of a launch of several waves of one-CTA units (both must fit the device).
+// tmk / tmv: one tensor map each, or p.num_sources of them for a fused tiled run.
 template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8>
-cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p,
+cudaError_t launch_unit(const CUtensorMap *tmk, const CUtensorMap *tmv, const UnitParams &p,
                         long long units, int stages_seq, cudaStream_t stream, int layout);
 
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream, bool programmatic);
+
+// Fold of a fused tiled run's per-call partials, in call order, into the
+// running state (from begin's (-inf, 0, 0)), then out = o / l.
+struct RunMergeParams {
+    const float *ws_o;   // [rows, num_sources, D]
+    const float *ws_ml;  // [rows, num_sources, 2]
+    const int32_t *src_counts[kMaxRunSources];
+    float *st_m, *st_l, *st_o;
+    __nv_bfloat16 *out;
+    int num_seqs, num_q_heads, head_dim, num_sources, tile_capacity;
+};
+cudaError_t launch_tiled_run_merge(const RunMergeParams &p, cudaStream_t stream);
 cudaError_t launch_tiled_begin(float *m, float *l, float *o, int rows, int head_dim,
                                cudaStream_t stream);
 cudaError_t launch_tiled_finalize(const float *l, const float *o, __nv_bfloat16 *out, int rows,

@@ -91,6 +91,71 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
     *reinterpret_cast<uint2 *>(p.out + row * D + d0) = pk;
 }
 
+// A fused tiled run's fold (tiled_attention.rs page: begin_step, one step_tile
+// per call, finalize): each row starts from begin's (-inf, 0, 0), folds the
+// calls' partials in call order with the same pinned rounding as step_tile's
+// own fold, skipping calls whose tile held no block, writes the state and
+// then out = o / l as BF16 (0 where l is 0), as finalize does.  One warp per
+// (row, 128 columns); every load of a row is issued together.
+__global__ void __launch_bounds__(kMergeWarps * 32) tiled_run_merge_kernel(const __grid_constant__ RunMergeParams p) {
+    const float kNegInf = -__int_as_float(0x7f800000);
+    dev::griddep_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int D = p.head_dim;
+    const int T = p.num_sources;
+    const int chunks = (D + kMergeCols - 1) / kMergeCols;
+    const long long item = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
+    if (item >= static_cast<long long>(p.num_seqs) * p.num_q_heads * chunks) return;
+    const long long row = item / chunks;
+    const int chunk = static_cast<int>(item - row * chunks);
+    const int d0 = chunk * kMergeCols + lane * 4;
+    const bool cols = d0 < D;  // D is a multiple of 8: the lane's 4 columns are all in range
+    dev::griddep_wait();  // the unit pass's partials are complete and visible
+    const int s = static_cast<int>(row / p.num_q_heads);
+    int cnt[kMaxRunSources];
+    float2 mli[kMaxRunSources];
+    float4 oi[kMaxRunSources];
+#pragma unroll
+    for (int c = 0; c < kMaxRunSources; ++c) {
+        if (c < T) {
+            cnt[c] = p.src_counts[c][s];
+            mli[c] = *reinterpret_cast<const float2 *>(p.ws_ml + (row * T + c) * 2);
+            oi[c] = cols ? *reinterpret_cast<const float4 *>(p.ws_o + (row * T + c) * D + d0)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    float m = kNegInf, l = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < kMaxRunSources; ++c) {
+        if (c < T && cnt[c] > 0) {
+            const float M = mli[c].x;
+            const float m_new = fmaxf(m, M);
+            const float fa = m == kNegInf ? 0.f : dev::exp2_approx(m - m_new);
+            const float fb = M == kNegInf ? 0.f : dev::exp2_approx(M - m_new);
+            l = dev::fold_value(l, fa, mli[c].y, fb);
+            o.x = dev::fold_value(o.x, fa, oi[c].x, fb);
+            o.y = dev::fold_value(o.y, fa, oi[c].y, fb);
+            o.z = dev::fold_value(o.z, fa, oi[c].z, fb);
+            o.w = dev::fold_value(o.w, fa, oi[c].w, fb);
+            m = m_new;
+        }
+    }
+    if (chunk == 0 && lane == 0) {
+        p.st_m[row] = m;
+        p.st_l[row] = l;
+    }
+    if (!cols) return;
+    *reinterpret_cast<float4 *>(p.st_o + row * D + d0) = o;
+    const bool pos = l > 0.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(pos ? __fdiv_rn(o.x, l) : 0.f, pos ? __fdiv_rn(o.y, l) : 0.f);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(pos ? __fdiv_rn(o.z, l) : 0.f, pos ? __fdiv_rn(o.w, l) : 0.f);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p.out + row * D + d0) = pk;
+}
+
 // TiledAttention::begin_step: (m, l, o) <- (-inf, 0, 0) over `rows` rows.
 __global__ void tiled_begin_kernel(float *m, float *l, float *o, long long rows, long long n_o) {
     const float kNegInf = -__int_as_float(0x7f800000);
@@ -141,6 +206,22 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream, bool program
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, merge_kernel, p);
+}
+
+cudaError_t launch_tiled_run_merge(const RunMergeParams &p, cudaStream_t stream) {
+    const long long items = static_cast<long long>(p.num_seqs) * p.num_q_heads *
+                            ((p.head_dim + kMergeCols - 1) / kMergeCols);
+    if (items == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((items + kMergeWarps - 1) / kMergeWarps));
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tiled_run_merge_kernel, p);
 }
 
 cudaError_t launch_tiled_begin(float *m, float *l, float *o, int rows, int head_dim,

@@ -57,20 +57,6 @@ constexpr unsigned int kDevBadContextLen = 2;
 constexpr unsigned int kDevBadTileCount = 4;
 constexpr unsigned int kDevWaitTimeout = 8;
 
-// Left fold of two (m, l, o) states in base 2: the running state R and the
-// next part P give M = max(mR, mP), a = 2^(mR - M), b = 2^(mP - M) (0 for an
-// empty side), l = lR*a + lP*b, o = oR*a + oP*b.  Rounding is pinned (no
-// contraction) so that every place that folds computes the same bits.
-__device__ __forceinline__ void fold_factors(float mr, float mp, float &mn, float &a, float &b) {
-    const float kNegInf = -__int_as_float(0x7f800000);
-    mn = fmaxf(mr, mp);
-    a = mr == kNegInf ? 0.f : dev::exp2_approx(mr - mn);
-    b = mp == kNegInf ? 0.f : dev::exp2_approx(mp - mn);
-}
-__device__ __forceinline__ float fold_value(float r, float a, float pv, float b) {
-    return __fadd_rn(__fmul_rn(r, a), __fmul_rn(pv, b));
-}
-
 // Shared-memory plan of a unit CTA (host and device agree on it).  Offsets are
 // from the 1024-byte-aligned base.  The warp-merge area and the CTA result
 // reuse the stage ring once every tile has been consumed.
@@ -155,13 +141,14 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 
 template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8>
 __global__ void __launch_bounds__(kThreads)
-    unit_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+    unit_kernel(const __grid_constant__ KvMaps<MODE == kModeTiledRun ? kMaxRunSources : 1> maps,
                 const __grid_constant__ UnitParams p) {
     constexpr int KS = DPAD / 16;      // mma k-steps of K.q^T == m-tiles of V^T.P^T
     constexpr int NBOX = DPAD / kBoxCols;                 // BF16 boxes per tile (64 columns each)
     constexpr int TILE_BYTES = kTileTokens * DPAD * (KV8 ? 1 : 2);  // one landed K or V tile
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static_assert(!KV8 || MODE == kModePaged, "FP8 caches are a paged-mode source");
+    constexpr bool RUN = MODE == kModeTiledRun;
     constexpr int RT = 8 * GN;         // query rows per CTA
     constexpr int OSTRIDE = DPAD + 4;  // padded row stride of o in shared memory
     constexpr int QST = DPAD * 2 + 16; // padded row stride of q in shared memory (bytes)
@@ -192,8 +179,6 @@ __global__ void __launch_bounds__(kThreads)
     // Shared-memory set-up needs no global memory: do it before waiting for
     // the previous kernel in the stream.
     if (tid == 0) {
-        dev::prefetch_tensormap(&tmk);
-        dev::prefetch_tensormap(&tmv);
         for (int i = 0; i < 2 * kWarps * S; ++i) dev::mbar_init(dev::smem_addr(&bars[i]), 1);
         dev::mbar_init(dev::smem_addr(bar_ready), kMaxParts);
         dev::mbar_init(dev::smem_addr(bar_done), kMaxParts);
@@ -208,10 +193,20 @@ __global__ void __launch_bounds__(kThreads)
     const int C = p.cluster;
     const int part = blockIdx.x % C;
     int u = blockIdx.x / C;
-    int split = 0;
+    int split = 0;  // paged: the split; fused tiled run: the source (step_tile call)
     if constexpr (MODE == kModePaged) {
         split = u % p.num_splits;
         u /= p.num_splits;
+    } else if constexpr (RUN) {
+        split = u % p.num_sources;
+        u /= p.num_sources;
+    }
+    const CUtensorMap *tmk = &maps.k[RUN ? split : 0];
+    const CUtensorMap *tmv = &maps.v[RUN ? split : 0];
+    const int tok_dim = RUN ? p.src_tok_dim[split] : p.tok_dim;
+    if (tid == 0) {
+        dev::prefetch_tensormap(tmk);
+        dev::prefetch_tensormap(tmv);
     }
     const int qt = u % p.qtiles;
     u /= p.qtiles;
@@ -254,7 +249,7 @@ __global__ void __launch_bounds__(kThreads)
     // prefetched early is never stale).  Everything is read again after the
     // wait.  This fills the DRAM idle time at the previous kernel's tail.  The
     // tiled step's tile counts and tile lists are treated the same way.
-    if (p.prefetch_tiles > 0) {
+    if (!RUN && p.prefetch_tiles > 0) {
         int t0 = 0, t1 = 0, ss = s;
         const int32_t *ids;
         if constexpr (MODE == kModePaged) {
@@ -286,12 +281,12 @@ __global__ void __launch_bounds__(kThreads)
                     const int id = __ldcg(ids + gt / tiles_per_block);
                     if (id >= 0 && id < p.num_blocks) {
                         const int sub = (gt % tiles_per_block) * kTileTokens;
-                        const int c1 = p.tok_dim == 1 ? sub : kvh;
-                        const int c2 = p.tok_dim == 1 ? kvh : sub;
+                        const int c1 = tok_dim == 1 ? sub : kvh;
+                        const int c2 = tok_dim == 1 ? kvh : sub;
 #pragma unroll
                         for (int b = 0; b < (KV8 ? 1 : NBOX); ++b) {
-                            dev::tma_prefetch_4d(&tmk, b * kBoxCols, c1, c2, id);
-                            dev::tma_prefetch_4d(&tmv, b * kBoxCols, c1, c2, id);
+                            dev::tma_prefetch_4d(tmk, b * kBoxCols, c1, c2, id);
+                            dev::tma_prefetch_4d(tmv, b * kBoxCols, c1, c2, id);
                         }
                     }
                 }
@@ -353,17 +348,20 @@ __global__ void __launch_bounds__(kThreads)
             return;  // uniform across the cluster: every rank sees the same range
         }
     } else {
-        int cnt = p.tile_counts[s];
+        // tiled step, or one call of a fused run: the call's tile list
+        const int32_t *counts = RUN ? p.src_counts[split] : p.tile_counts;
+        int cnt = counts[s];
         if (cnt < 0 || cnt > p.tile_capacity) {
             if (tid == 0 && part == 0 && qt == 0 && kvh == 0)
                 dev::flag_status(p.status, kDevBadTileCount);
             cnt = cnt < 0 ? 0 : p.tile_capacity;
         }
         if (cnt == 0) return;  // nothing to fold: the state is unchanged
-        const int lv = (p.last_valid >= 1 && p.last_valid < bs) ? p.last_valid : bs;
+        const int lvc = RUN ? p.src_last_valid[split] : p.last_valid;
+        const int lv = (lvc >= 1 && lvc < bs) ? lvc : bs;
         tok0 = 0;
         tok1 = (cnt - 1) * bs + lv;
-        ids_base = p.tile_blocks + static_cast<long long>(s) * p.tile_capacity;
+        ids_base = (RUN ? p.src_blocks[split] : p.tile_blocks) + static_cast<long long>(s) * p.tile_capacity;
     }
 
     // 16-token tiles of the range, cut into V parts of about p.part_tiles tiles
@@ -486,8 +484,8 @@ __global__ void __launch_bounds__(kThreads)
             const int sub = (gt % tiles_per_block) * kTileTokens;
             const uint32_t bar = dev::smem_addr(&bars[(warp * S + k) * 2 + half]);
             const uint32_t dst = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES + half * TILE_BYTES);
-            const int c1 = p.tok_dim == 1 ? sub : kvh;
-            const int c2 = p.tok_dim == 1 ? kvh : sub;
+            const int c1 = tok_dim == 1 ? sub : kvh;
+            const int c2 = tok_dim == 1 ? kvh : sub;
             dev::mbar_arrive_expect_tx(bar, TILE_BYTES);
             // BF16: NBOX swizzled boxes of 64 columns; FP8: one unswizzled box of the whole row
 #pragma unroll
@@ -509,8 +507,8 @@ __global__ void __launch_bounds__(kThreads)
         for (int r = 0; r < npro; ++r) {
             const int id = __shfl_sync(0xffffffffu, id_cur, r);
             if (lane == 0) {
-                issue(&tmk, 0, r, (rr + r) % S, id);
-                issue(&tmv, 1, r, (rr + r) % S, id);
+                issue(tmk, 0, r, (rr + r) % S, id);
+                issue(tmv, 1, r, (rr + r) % S, id);
             }
         }
 
@@ -573,8 +571,8 @@ __global__ void __launch_bounds__(kThreads)
                 e4m3_tile_to_f16<DPAD>(stage + TILE_BYTES, cvt + kTileTokens * DPAD * 2, lane);
                 __syncwarp();
                 if (rn < nloc && lane == 0) {
-                    issue(&tmk, 0, rn, k, id_next);
-                    issue(&tmv, 1, rn, k, id_next);
+                    issue(tmk, 0, rn, k, id_next);
+                    issue(tmv, 1, rn, k, id_next);
                 }
                 kbase = dev::smem_addr(cvt);
                 vbase = kbase + kTileTokens * DPAD * 2;
@@ -583,7 +581,7 @@ __global__ void __launch_bounds__(kThreads)
                 __syncwarp();  // the previous tile's reads of the f16 tile are done
                 e4m3_tile_to_f16<DPAD>(stage, cvt, lane);
                 __syncwarp();
-                if (rn < nloc && lane == 0) issue(&tmk, 0, rn, k, id_next);
+                if (rn < nloc && lane == 0) issue(tmk, 0, rn, k, id_next);
                 kbase = dev::smem_addr(cvt);
                 vbase = kbase;
             }
@@ -613,7 +611,7 @@ __global__ void __launch_bounds__(kThreads)
             if constexpr (!KV8) {
                 if (rn < nloc) {
                     __syncwarp();
-                    if (lane == 0) issue(&tmk, 0, rn, k, id_next);
+                    if (lane == 0) issue(tmk, 0, rn, k, id_next);
                 }
             }
 
@@ -714,7 +712,7 @@ __global__ void __launch_bounds__(kThreads)
                 __syncwarp();
                 e4m3_tile_to_f16<DPAD>(stage + TILE_BYTES, cvt, lane);
                 __syncwarp();
-                if (rn < nloc && lane == 0) issue(&tmv, 1, rn, k, id_next);
+                if (rn < nloc && lane == 0) issue(tmv, 1, rn, k, id_next);
             }
             // O^T += V^T . P^T  (V rows past the range may hold anything: mask them)
             auto pv_tile = [&](uint32_t mask01, uint32_t mask89) {
@@ -744,7 +742,7 @@ __global__ void __launch_bounds__(kThreads)
             if constexpr (!KV8) {
                 if (rn < nloc) {
                     __syncwarp();
-                    if (lane == 0) issue(&tmv, 1, rn, k, id_next);
+                    if (lane == 0) issue(tmv, 1, rn, k, id_next);
                 }
             }
         }
@@ -831,8 +829,8 @@ __global__ void __launch_bounds__(kThreads)
             __syncthreads();
             if (tid < Gt) {
                 float Mn, fa, fb;
-                fold_factors(rM[tid], cm[tid], Mn, fa, fb);
-                rL[tid] = fold_value(rL[tid], fa, cl[tid], fb);
+                dev::fold_factors(rM[tid], cm[tid], Mn, fa, fb);
+                rL[tid] = dev::fold_value(rL[tid], fa, cl[tid], fb);
                 rM[tid] = Mn;
                 fx[tid * 4 + 2] = fa;
                 fx[tid * 4 + 3] = fb;
@@ -842,7 +840,7 @@ __global__ void __launch_bounds__(kThreads)
             for (int i = 0; i < RACC; ++i) {
                 const int e = tid + i * kThreads;
                 const int g = e / DPAD, d = e - g * DPAD;
-                if (g < Gt) racc[i] = fold_value(racc[i], fx[g * 4 + 2], co[g * OSTRIDE + d], fx[g * 4 + 3]);
+                if (g < Gt) racc[i] = dev::fold_value(racc[i], fx[g * 4 + 2], co[g * OSTRIDE + d], fx[g * 4 + 3]);
             }
             __syncthreads();  // the ring (and co over it) is free for the next part
         }
@@ -906,8 +904,8 @@ __global__ void __launch_bounds__(kThreads)
                 const float mj = cluster.map_shared_rank(cm, jj)[g];
                 const float lj = cluster.map_shared_rank(cl, jj)[g];
                 float Mn, fa, fb;
-                fold_factors(M, mj, Mn, fa, fb);
-                Lsum = fold_value(Lsum, fa, lj, fb);
+                dev::fold_factors(M, mj, Mn, fa, fb);
+                Lsum = dev::fold_value(Lsum, fa, lj, fb);
                 M = Mn;
                 fr[tid * 2 * kMaxParts + 2 * jj + 0] = fa;
                 fr[tid * 2 * kMaxParts + 2 * jj + 1] = fb;
@@ -918,19 +916,22 @@ __global__ void __launch_bounds__(kThreads)
         }
         const long long row = static_cast<long long>(s) * Hq + h0 + g;
         float fa = 0.f, fb = 0.f;
-        if constexpr (MODE == kModePaged) {
-            if (!direct) {
+        if constexpr (MODE == kModePaged || RUN) {
+            // a split's, or a fused run's call's, partial [o, m, l]
+            if (RUN || !direct) {
                 p.ws_ml[(row * p.num_splits + split) * 2 + 0] = M;
                 p.ws_ml[(row * p.num_splits + split) * 2 + 1] = Lsum;
             } else {
                 fb = Lsum > 0.f ? 1.f : 0.f;
             }
         } else {
+            // TiledAttention::step_tile: fold into the running state (the fused
+            // run's merge replays exactly this, in call order)
             const float m_old = p.st_m[row];
             const float m_new = fmaxf(m_old, M);
             fa = m_old == kNegInf ? 0.f : dev::exp2_approx(m_old - m_new);
             fb = M == kNegInf ? 0.f : dev::exp2_approx(M - m_new);
-            p.st_l[row] = p.st_l[row] * fa + Lsum * fb;
+            p.st_l[row] = dev::fold_value(p.st_l[row], fa, Lsum, fb);
             p.st_m[row] = m_new;
         }
         fx[tid * 4 + 0] = M;
@@ -962,8 +963,8 @@ __global__ void __launch_bounds__(kThreads)
                 if (jj < V) {
                     const float fa = fr[i * 2 * kMaxParts + 2 * jj + 0];
                     const float fb = fr[i * 2 * kMaxParts + 2 * jj + 1];
-                    acc0 = fold_value(acc0, fa, v0[jj], fb);
-                    acc1 = fold_value(acc1, fa, v1[jj], fb);
+                    acc0 = dev::fold_value(acc0, fa, v0[jj], fb);
+                    acc1 = dev::fold_value(acc1, fa, v1[jj], fb);
                 }
             }
         } else {
@@ -975,8 +976,8 @@ __global__ void __launch_bounds__(kThreads)
             acc0 *= p.v_scale;
             acc1 *= p.v_scale;
         }
-        if constexpr (MODE == kModePaged) {
-            if (direct) {
+        if constexpr (MODE == kModePaged || RUN) {
+            if (!RUN && direct) {
                 const float Lsum = fx[i * 4 + 1];
                 const bool pos = fx[i * 4 + 3] > 0.f;
                 const __nv_bfloat162 v = __floats2bfloat162_rn(pos ? __fdiv_rn(acc0, Lsum) : 0.f,
@@ -990,8 +991,8 @@ __global__ void __launch_bounds__(kThreads)
             const float fa = fx[i * 4 + 2], fb = fx[i * 4 + 3];
             float2 *so = reinterpret_cast<float2 *>(p.st_o + row * D + d);
             float2 cur = *so;
-            cur.x = cur.x * fa + acc0 * fb;
-            cur.y = cur.y * fa + acc1 * fb;
+            cur.x = dev::fold_value(cur.x, fa, acc0, fb);
+            cur.y = dev::fold_value(cur.y, fa, acc1, fb);
             *so = cur;
         }
     }

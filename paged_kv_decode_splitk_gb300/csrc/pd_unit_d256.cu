@@ -7,6 +7,9 @@ PD_INSTANTIATE_UNIT(256, 2, false, pd::kModePaged, false, false)
 PD_INSTANTIATE_UNIT(256, 1, true, pd::kModeTiled, false, false)
 PD_INSTANTIATE_UNIT(256, 1, false, pd::kModeTiled, false, false)
 PD_INSTANTIATE_UNIT(256, 2, false, pd::kModeTiled, false, false)
+PD_INSTANTIATE_UNIT(256, 1, true, pd::kModeTiledRun, false, false)
+PD_INSTANTIATE_UNIT(256, 1, false, pd::kModeTiledRun, false, false)
+PD_INSTANTIATE_UNIT(256, 2, false, pd::kModeTiledRun, false, false)
 
 // The GQA-packed pass: group width PD_GQA at head dim PD_HDIM, compile-time.
 PD_INSTANTIATE_UNIT(PD_HDIM, 1, false, pd::kModePaged, true, false)

@@ -7,3 +7,6 @@ PD_INSTANTIATE_UNIT(64, 2, false, pd::kModePaged, false, false)
 PD_INSTANTIATE_UNIT(64, 1, true, pd::kModeTiled, false, false)
 PD_INSTANTIATE_UNIT(64, 1, false, pd::kModeTiled, false, false)
 PD_INSTANTIATE_UNIT(64, 2, false, pd::kModeTiled, false, false)
+PD_INSTANTIATE_UNIT(64, 1, true, pd::kModeTiledRun, false, false)
+PD_INSTANTIATE_UNIT(64, 1, false, pd::kModeTiledRun, false, false)
+PD_INSTANTIATE_UNIT(64, 2, false, pd::kModeTiledRun, false, false)

@@ -2,6 +2,7 @@
 // per-head-dim translation units that instantiate it.
 #pragma once
 
+#include <cstring>
 #include <mutex>
 
 #include "pd_unit.cuh"
@@ -9,7 +10,7 @@
 namespace pd {
 
 template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8>
-cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const UnitParams &p_in,
+cudaError_t launch_unit(const CUtensorMap *tmk, const CUtensorMap *tmv, const UnitParams &p_in,
                         long long units, int stages_seq, cudaStream_t stream, int layout) {
     auto kern = unit_kernel<DPAD, GN, HL, MODE, PACKED, KV8>;
     // Per device: the dynamic shared-memory limit raised so far, the SM count,
@@ -98,12 +99,21 @@ cudaError_t launch_unit(const CUtensorMap &tmk, const CUtensorMap &tmv, const Un
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, p);
+    constexpr int NM = MODE == kModeTiledRun ? kMaxRunSources : 1;
+    const int nmaps = MODE == kModeTiledRun ? p.num_sources : 1;
+    if (nmaps < 1 || nmaps > NM) return cudaErrorInvalidValue;
+    KvMaps<NM> maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int i = 0; i < nmaps; ++i) {
+        maps.k[i] = tmk[i];
+        maps.v[i] = tmv[i];
+    }
+    return cudaLaunchKernelEx(&cfg, kern, maps, p);
 }
 
 }  // namespace pd
 
 #define PD_INSTANTIATE_UNIT(DPAD, GN, HL, MODE, PACKED, KV8)                                 \
     template cudaError_t pd::launch_unit<DPAD, GN, HL, MODE, PACKED, KV8>(                   \
-        const CUtensorMap &, const CUtensorMap &, const pd::UnitParams &, long long, int,       \
+        const CUtensorMap *, const CUtensorMap *, const pd::UnitParams &, long long, int,       \
         cudaStream_t, int);

@@ -160,3 +160,25 @@ def test_tiled_run_checks_every_source_before_launching(cuda_device):
         assert bool(torch.all(out == 0))
     finally:
         t.close()
+
+
+def test_fused_tiled_run_reports_allocation_failure(cuda_device):
+    """The first fused pd_tiled_run allocates the handle's partials buffer: an
+    injected failure is reported as PD_ERR_ALLOC, and the next run succeeds."""
+    mw = W.tiled_mixed(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_dim=64, tile_capacity=8,
+                       max_blocks=16, seed=58)
+    inp = api.MixedTiledInputs(mw, cuda_device)
+    t = pd.Tiled(3, 8, 2, 64, 16, 8)
+    try:
+        out = torch.empty((3, 8, 64), dtype=torch.bfloat16, device=cuda_device)
+        pd.pd_debug_fail_next_allocs(1)
+        with pytest.raises(pd.PdError) as e:
+            t.run(inp.q, inp.sources(t), out, 3)
+        assert e.value.code == pd.PD_ERR_ALLOC
+        pd.pd_debug_fail_next_allocs(0)
+        t.run(inp.q, inp.sources(t), out, 3)
+        torch.cuda.synchronize()
+        assert pd.pd_device_status() == 0
+    finally:
+        pd.pd_debug_fail_next_allocs(0)
+        t.close()
