@@ -261,7 +261,14 @@ constexpr int kPartTiles = 32;
 // L2 before it waits for the previous kernel (a scheduling hint: it changes no
 // result); a 16-token K+V tile holds 64 * dpad bytes.
 constexpr int kPrefetchBytes = 128 * 1024;
-int max_parts_for(int dpad, bool tiled) { return tiled ? 2 : (dpad >= 256 ? 8 : 4); }
+// Cluster sizes: 8 at D = 256; at D <= 128 five for BF16 (a 158-tile split in
+// 5 CTAs of 4 warps still fits one wave at 4 CTAs per SM: measured 27.3 ->
+// 26.9 us on the long-context workload), four for FP8 (3 CTAs per SM there).
+int max_parts_for(int dpad, bool tiled, bool kv8 = false) {
+    if (tiled) return 2;
+    if (dpad >= 256) return 8;
+    return kv8 ? 4 : 5;
+}
 
 int dpad_for(int head_dim) { return head_dim <= 64 ? 64 : (head_dim <= 128 ? 128 : 256); }
 
@@ -541,7 +548,7 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     const int qtiles = (G + rows - 1) / rows;
     const int stages = default_stages(dpad, kv8);
     const long long units = static_cast<long long>(num_seqs) * num_kv_heads * qtiles * num_splits;
-    if (units * max_parts_for(dpad, false) > 0x7fffffffLL)
+    if (units * max_parts_for(dpad, false, kv8) > 0x7fffffffLL)
         return fail(PD_ERR_INVALID, "launch too large (%lld units)", units);
 
     int err = PD_OK;
@@ -582,7 +589,7 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     p.block_size = block_size;
     p.qtiles = qtiles;
     p.cluster = 1;
-    p.max_parts = max_parts_for(dpad, false);
+    p.max_parts = max_parts_for(dpad, false, kv8);
     p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = default_lpt(num_seqs);
