@@ -360,8 +360,13 @@ typedef struct pd_tiled_source {
  * source is checked before anything launches, so an invalid argument leaves
  * the running state and `out` untouched.  The result equals one begin, the
  * steps and one finalize made separately (same kernels, same order).
- * num_sources may be 0 (out = 0).  Returns PD_OK, PD_ERR_CAPACITY,
- * PD_ERR_INVALID or PD_ERR_CUDA. */
+ * num_sources may be 0 (out = 0).  With 1..8 sources the step runs as two
+ * launches (every call's tile at once, then the in-order fold and finalize)
+ * instead of 2 + num_sources; the first such run on a handle allocates the
+ * handle's partials buffer (max_seqs * num_q_heads * 8 * (head_dim + 2)
+ * floats), so it must not be the first call inside a CUDA graph capture.
+ * Returns PD_OK, PD_ERR_CAPACITY, PD_ERR_INVALID, PD_ERR_ALLOC or
+ * PD_ERR_CUDA. */
 int pd_tiled_run(pd_tiled *t, const void *q, const pd_tiled_source *sources, int num_sources,
                  void *out, int num_seqs, void *stream);
 
