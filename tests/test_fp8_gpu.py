@@ -107,3 +107,10 @@ def test_fp8_argument_errors(cuda_device):
         pd.pd_decode_attn_fp8(i40.q, i40.k, i40.v, 1.0, 1.0, i40.block_table, i40.context_lens, out40,
                               w40.inv_sqrt_d, 1)
     assert e.value.code == pd.PD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("bs", [32, 64, 256])
+def test_fp8_block_sizes(cuda_device, bs):
+    w = W.fp8_variant(W.custom([0, 1, 31, 33, 500, 1100], 16, 4, 128, block_size=bs, seed=99), seed=bs)
+    got = _run(w, cuda_device, 3)
+    assert_within_tolerance(got, _ref(w), f"fp8 block {bs}")
