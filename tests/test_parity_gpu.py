@@ -57,6 +57,9 @@ EDGE_SHAPES = [
     ([77, 500, 1025], 8, 1, 128, 32, 3),         # block size 32
     ([77, 500, 1025], 8, 2, 128, 64, 4),         # block size 64
     ([0, 0, 0], 8, 2, 128, 16, 3),               # nothing at all
+    ([3000, 5, 256], 8, 2, 256, 256, 2),         # block size 256 at head dim 256, group 4
+    ([70000], 8, 1, 64, 16, 16),                 # one very long sequence at 16 splits
+    ([300, 9, 2600], 32, 2, 128, 16, 3),         # group 16 at head dim 128
 ]
 
 
