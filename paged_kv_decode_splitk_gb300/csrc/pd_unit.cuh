@@ -113,8 +113,15 @@ __device__ __forceinline__ void e4m3_tile_to_f16(const uint8_t *src, uint8_t *ds
     // a full unroll would hold every chunk's registers on top of the o accumulators
 #pragma unroll(DPAD <= 128 ? DPAD / 32 : 2)
     for (int i = 0; i < DPAD / 32; ++i) {
-        const int c = lane + 32 * i;
-        const int t = c / CPR, k = c - t * CPR;
+        // Iteration i covers rows 8*(i / (CPR/4)) .. +7; a quarter-warp takes 2
+        // rows x 4 chunks of one box (the second row the neighbouring box when
+        // there are two or more), so its eight 16-byte stores land in distinct
+        // swizzled positions and its loads in distinct banks (no conflict).
+        const int kb = i % (CPR / 4), rb = i / (CPR / 4);
+        const int q = lane >> 3, j = lane & 7;
+        const int kbx = CPR >= 8 ? (kb ^ (j >> 2)) : kb;
+        const int t = 8 * rb + 2 * q + (j >> 2), k = 4 * kbx + (j & 3);
+        const int c = t * CPR + k;
         const uint4 v = *reinterpret_cast<const uint4 *>(src + c * 16);
         uint4 lo, hi;
         dev::e4m3x4_to_f16x4(v.x, lo.x, lo.y);
