@@ -128,19 +128,30 @@ def job_value(kv_bytes_per_rank: int, steps: int, total_ms: float, world_size: i
     return world_size * kv_bytes_per_rank * steps / (total_ms / 1e3) / 1e9
 
 
+def source_digest() -> str:
+    """Hash of the kernel sources (paged_kv_decode_splitk_gb300/csrc) with their
+    comments and blank space removed: it changes when the code does."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_splitk_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"\s+", " ", text)
+        h.update(f.encode() + b"\0" + text.encode())
+    return h.hexdigest()[:16]
+
+
 def _traffic_from_profiles(kernel_tag: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    kernel source as it is now (the summary records a hash of the sources)."""
-    import hashlib
+    kernel code as it is now (the summary records source_digest())."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}__{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "paged_kv_decode_splitk_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
     tag = None
     traffic = None
     for ln in text.splitlines():
@@ -148,7 +159,7 @@ def _traffic_from_profiles(kernel_tag: str, workload: str):
             tag = ln.split(":", 1)[1].strip()
         if ln.startswith("dram_bytes_per_launch:"):
             traffic = float(ln.split(":", 1)[1].strip())
-    if tag != h.hexdigest()[:16]:
+    if tag != source_digest():
         return None
     return traffic
 

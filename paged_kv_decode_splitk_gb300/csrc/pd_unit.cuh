@@ -1,5 +1,8 @@
 // pd_unit.cuh -- the unit kernel: one (sequence, KV head, split) of paged-decode
 // attention, serving a whole group of query heads from one read of K and V.
+// The same kernel, by template mode, is the tiled step (one (sequence, KV
+// head) of a step_tile call) and the fused tiled run (one (sequence, KV head,
+// call) of every call at once).
 //
 // What a unit computes (Module attn_splitk page: split-K partials kept as
 // [o, m, l]; tiled_attention.rs page: the running (m, l, o) fold):
@@ -9,28 +12,39 @@
 //   (kept internally in base-2 units: m is max_t x[g,t]*log2(e)).
 //
 // GB300 mapping:
-//   * A CTA of kWarps warps owns a range of 16-token tiles.  Warp w folds tiles
-//     w, w+kWarps, ... with its own online-softmax state, then the warps merge
-//     in warp order through shared memory.  A unit may span a thread-block
-//     cluster of C CTAs that split the range and merge through distributed
-//     shared memory in rank order.  The range split, the warp interleave and
-//     both merge orders depend only on the unit's own length and build
-//     constants, so a sequence's bits never depend on the rest of the batch.
-//   * K and V tiles (16 tokens x head_dim BF16) move global -> shared with 4-D
-//     TMA tensor loads gathered through the block table (one box per 64
-//     columns, 128-byte swizzle).  Each warp runs a private ring of `stages`
-//     buffers with separate K and V mbarriers: the K half of a buffer is
-//     refilled as soon as q.K^T has read it, the V half after P.V, so the next
-//     tile's loads overlap the current tile's math.
-//   * Both products run on the tensor cores (mma.sync m16n8k16 BF16 -> FP32)
-//     with the tokens as the M dimension: S^T[t,g] = K[t,:] q[g,:]^T (the
-//     group fills N = 8), then O^T[d,g] += V^T[d,t] P^T[t,g].  P^T comes from
-//     the S^T accumulators through an in-register 8x8 transpose (movmatrix).
-//     P is split into a BF16 high part and a BF16 residual, which keeps ~16
-//     significant bits of every weight; for groups of at most 4 the residual
-//     rides in the otherwise idle columns 4..7 of the same mma.
+//   * The unit's range of 16-token tiles is cut into V length-defined parts
+//     (V = clamp(ceil(tiles / part_tiles), 1, max_parts)).  A CTA of kWarps
+//     warps takes a part; warp w folds its tiles w, w+kWarps, ... with its own
+//     online-softmax state and the warps merge in warp order.  The parts fold
+//     left to right with pinned rounding, either in one CTA walking them in
+//     turn or across a thread-block cluster (one part per rank, combined
+//     through distributed shared memory).  V, the warp interleave and every
+//     fold order depend only on the unit's own length and build constants,
+//     so a sequence's bits depend neither on the batch nor on the layout.
+//   * Cluster ranks beyond V leave at once; the others hand their parts over
+//     through mbarriers (bounded waits), or through the hardware cluster
+//     barrier when every rank holds a part.
+//   * K and V tiles move global -> shared with 4-D TMA tensor loads gathered
+//     through the block table (BF16: one 128-byte-swizzled box per 64
+//     columns; FP8 E4M3: one box of the padded row, converted by the warp to
+//     an f16 tile in the same swizzled layout).  Each warp runs a private ring
+//     of `stages` buffers with separate K and V mbarriers, refilled as soon
+//     as their data has been read, so the next tiles' loads overlap the
+//     current tile's math.
+//   * Both products run on the tensor cores (mma.sync m16n8k16, BF16 or f16
+//     operands, FP32 accumulate) with the tokens as the M dimension:
+//     S^T[t,g] = K[t,:] q[g,:]^T (the group fills N = 8), then
+//     O^T[d,g] += V^T[d,t] P^T[t,g].  P^T comes from the S^T accumulators
+//     through an in-register 8x8 transpose (movmatrix).  P is split into a
+//     high part and a residual, which keeps ~16 significant bits of every
+//     weight; for groups of at most 4 the residual rides in the otherwise
+//     idle columns 4..7 of the same mma.
 //   * Column max and column sums of S^T use warp shuffles over the 8 lanes
 //     that hold a column.
+//   * Before waiting for the previous kernel (programmatic dependent launch),
+//     a single-wave paged launch prefetches each CTA's first tiles into L2
+//     from speculative, L2-only reads of the lengths and block ids; nothing
+//     read before the wait feeds a result.
 #pragma once
 
 #include <cooperative_groups.h>
