@@ -395,7 +395,8 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            # the products' operand type: BF16, or f16 for an FP8 cache (converted exactly)
+            "dtype": "f16" if w.__dict__.get("kv_dtype") == "e4m3" else "bf16",
             "data": "synthetic (seeded N(0,1) BF16 q/K/V, seeded lengths and block tables)",
             "config": {
                 "workload": w.name,
