@@ -507,13 +507,20 @@ def _sample_seqs(w, budget_s):
 
 def cpu_baseline(w, workload, budget_s=10.0):
     seqs = _sample_seqs(w, budget_s)
+    # whole passes over the sample until the budget is spent (a workload that
+    # the oracle finishes quickly is timed over several passes)
+    passes = 0
     t0 = time.perf_counter()
-    _oracle_step(w, seqs)
-    dt = time.perf_counter() - t0
+    while True:
+        _oracle_step(w, seqs)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= 0.9 * budget_s:
+            break
     b = _seq_bytes(w, seqs)
-    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(seqs)} of {w.num_seqs} sequences of {workload} ({b / 1e6:.1f} MB of K/V), "
-                      f"FP64 C oracle, single thread, {dt:.1f} s"}
+    return {"value": round(b * passes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(seqs)} of {w.num_seqs} sequences of {workload} ({b / 1e6:.1f} MB of K/V) "
+                      f"x {passes} pass(es), FP64 C oracle, single thread, {dt:.1f} s"}
 
 
 def run_reference(args):
