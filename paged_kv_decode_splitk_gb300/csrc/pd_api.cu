@@ -127,11 +127,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 // else), so repeated launches over the same cache skip the host-side encode.
 struct KvMapKey {
     const void *base;
-    int head_dim, block_size, num_kv_heads, elem, box_cols;
+    int head_dim, block_size, num_kv_heads, elem, box_cols, swz128;
     long long num_blocks, blk_stride, tok_stride, kvh_stride;
     bool operator==(const KvMapKey &o) const {
         return base == o.base && head_dim == o.head_dim && block_size == o.block_size &&
-               num_kv_heads == o.num_kv_heads && elem == o.elem && box_cols == o.box_cols &&
+               num_kv_heads == o.num_kv_heads && elem == o.elem && box_cols == o.box_cols && swz128 == o.swz128 &&
                num_blocks == o.num_blocks && blk_stride == o.blk_stride && tok_stride == o.tok_stride &&
                kvh_stride == o.kvh_stride;
     }
@@ -150,16 +150,18 @@ unsigned long long g_map_clock = 0;
 int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int head_dim,
                            int block_size, int num_kv_heads, long long num_blocks,
                            long long blk_stride, long long tok_stride, long long kvh_stride, int elem,
-                           int box_cols);
+                           int box_cols, int swz128);
 
-// 4-D tensor map of a K or V view (strides in elements).  elem 2: BF16, boxes
-// of 64 columns with the 128-byte swizzle; elem 1: FP8 E4M3 codes, one
-// unswizzled box of box_cols columns (the padded head dim) per tile.
+// 4-D tensor map of a K or V view (strides in elements), boxes of box_cols
+// columns x 16 tokens.  elem 2: BF16, 64 columns with the 128-byte swizzle;
+// elem 1: FP8 E4M3 codes, either 128 columns with the 128-byte swizzle (the K
+// operand read straight from the tile) or one unswizzled box of the padded head
+// dim (V, converted to f16 first; every FP8 tile at head dim 64).
 int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim, int block_size,
                   int num_kv_heads, long long num_blocks, long long blk_stride, long long tok_stride,
-                  long long kvh_stride, int elem = 2, int box_cols = pd::kBoxCols) {
-    const KvMapKey key = {base, head_dim, block_size, num_kv_heads, elem, box_cols, num_blocks, blk_stride,
-                          tok_stride, kvh_stride};
+                  long long kvh_stride, int elem = 2, int box_cols = pd::kBoxCols, int swz128 = 1) {
+    const KvMapKey key = {base, head_dim, block_size, num_kv_heads, elem, box_cols, swz128, num_blocks,
+                          blk_stride, tok_stride, kvh_stride};
     std::lock_guard<std::mutex> lock(g_map_mu);
     int victim = 0;
     for (int i = 0; i < kMapCache; ++i) {
@@ -172,7 +174,7 @@ int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim
         if (g_maps[i].stamp < g_maps[victim].stamp) victim = i;
     }
     int rc = encode_kv_map_uncached(map, tok_dim, base, head_dim, block_size, num_kv_heads, num_blocks,
-                                    blk_stride, tok_stride, kvh_stride, elem, box_cols);
+                                    blk_stride, tok_stride, kvh_stride, elem, box_cols, swz128);
     if (rc != PD_OK) return rc;
     g_maps[victim].key = key;
     g_maps[victim].map = *map;
@@ -184,7 +186,7 @@ int encode_kv_map(CUtensorMap *map, int *tok_dim, const void *base, int head_dim
 int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int head_dim,
                            int block_size, int num_kv_heads, long long num_blocks,
                            long long blk_stride, long long tok_stride, long long kvh_stride, int elem,
-                           int box_cols) {
+                           int box_cols, int swz128) {
     auto enc = encoder();
     if (!enc) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled entry point");
     const bool tok_first = tok_stride <= kvh_stride;
@@ -214,7 +216,7 @@ int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int
     box[3] = 1;
     CUresult r = enc(map, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                      const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     elem == 1 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                     swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PD_ERR_INVALID,
@@ -560,12 +562,16 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     const long long kvh_s = head_dim, tok_s = static_cast<long long>(num_kv_heads) * head_dim;
     const long long blk_s = tok_s * block_size;
     const int elem = kv8 ? 1 : 2;
-    const int box_cols = kv8 ? dpad : pd::kBoxCols;
+    // FP8 from head dim 128 up: K in 128-code swizzled boxes (read straight into
+    // the mma operands), V in one unswizzled box of the padded row
+    const bool k_direct = kv8 && dpad >= 128;
+    const int box_k = !kv8 ? pd::kBoxCols : (k_direct ? 128 : dpad);
+    const int box_v = kv8 ? dpad : pd::kBoxCols;
     rc = encode_kv_map(&tk, &tok_dim, k_cache, head_dim, block_size, num_kv_heads, num_blocks, blk_s,
-                       tok_s, kvh_s, elem, box_cols);
+                       tok_s, kvh_s, elem, box_k, !kv8 || k_direct);
     if (rc != PD_OK) return rc;
     rc = encode_kv_map(&tv, &tok_dim, v_cache, head_dim, block_size, num_kv_heads, num_blocks, blk_s,
-                       tok_s, kvh_s, elem, box_cols);
+                       tok_s, kvh_s, elem, box_v, !kv8);
     if (rc != PD_OK) return rc;
 
     pd::UnitParams p = {};

@@ -145,6 +145,10 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, 
                  : "memory");
 }
 
+__device__ __forceinline__ void lds_v2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
                  : "=r"(r0), "=r"(r1)

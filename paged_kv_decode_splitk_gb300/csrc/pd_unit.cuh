@@ -26,8 +26,11 @@
 //     barrier when every rank holds a part.
 //   * K and V tiles move global -> shared with 4-D TMA tensor loads gathered
 //     through the block table (BF16: one 128-byte-swizzled box per 64
-//     columns; FP8 E4M3: one box of the padded row, converted by the warp to
-//     an f16 tile in the same swizzled layout).  Each warp runs a private ring
+//     columns; FP8 E4M3 from head dim 128 up: K in 128-byte-swizzled boxes of
+//     128 codes whose codes each thread converts straight into its mma
+//     operands, V in one box of the padded row converted by the warp to an
+//     f16 tile in the BF16 layout; at head dim 64 both go through f16 tiles).
+//     Each warp runs a private ring
 //     of `stages` buffers with separate K and V mbarriers, refilled as soon
 //     as their data has been read, so the next tiles' loads overlap the
 //     current tile's math.
@@ -101,7 +104,9 @@ __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stage
     const int result = rows * ostride * 4;
     s.stages = 0;
     s.cvt = (ring + 1023) / 1024 * 1024;
-    const int cvt_tiles = dpad <= 128 ? 2 : 1;  // K and V apart, or one tile shared in turn
+    // f16 tiles per warp: K and V apart at head dims up to 64; from 128 up only
+    // V is converted (K's codes go straight into the mma operands)
+    const int cvt_tiles = dpad <= 64 ? 2 : 1;
     const int loop_end = kv8 ? s.cvt + kWarps * cvt_tiles * kTileTokens * dpad * 2 : ring;
     s.merge = 0;
     s.result = merge;
@@ -166,6 +171,9 @@ __global__ void __launch_bounds__(kThreads)
                 const __grid_constant__ UnitParams p) {
     constexpr int KS = DPAD / 16;      // mma k-steps of K.q^T == m-tiles of V^T.P^T
     constexpr int NBOX = DPAD / kBoxCols;                 // BF16 boxes per tile (64 columns each)
+    // FP8 cache from head dim 128 up: K's codes go from the (128-byte swizzled)
+    // FP8 tile straight into the mma operands; only V passes through an f16 tile.
+    constexpr bool KDIRECT = KV8 && DPAD >= 128;
     constexpr int TILE_BYTES = kTileTokens * DPAD * (KV8 ? 1 : 2);  // one landed K or V tile
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static_assert(!KV8 || MODE == kModePaged, "FP8 caches are a paged-mode source");
@@ -306,8 +314,12 @@ __global__ void __launch_bounds__(kThreads)
                         const int c2 = tok_dim == 1 ? kvh : sub;
 #pragma unroll
                         for (int b = 0; b < (KV8 ? 1 : NBOX); ++b) {
-                            dev::tma_prefetch_4d(tmk, b * kBoxCols, c1, c2, id);
                             dev::tma_prefetch_4d(tmv, b * kBoxCols, c1, c2, id);
+                            if constexpr (!KDIRECT) dev::tma_prefetch_4d(tmk, b * kBoxCols, c1, c2, id);
+                        }
+                        if constexpr (KDIRECT) {
+#pragma unroll
+                            for (int b = 0; b < DPAD / 128; ++b) dev::tma_prefetch_4d(tmk, b * 128, c1, c2, id);
                         }
                     }
                 }
@@ -422,7 +434,13 @@ __global__ void __launch_bounds__(kThreads)
         for (int i = 0; i < QPT; ++i) {
             const int e = tid + i * kThreads;
             const int g = e / (DPAD / 2);
-            const int d = (e - g * (DPAD / 2)) * 2;
+            int d = (e - g * (DPAD / 2)) * 2;
+            if constexpr (KDIRECT) {
+                // column pair P of a 32-column block sits where the direct K
+                // operand uses it: pair 4*qd + 2*h + hi -> k-step h, pair qd + 4*hi
+                const int P = d >> 1, pp = P & 15;
+                d = ((P & ~15) + ((pp >> 1) & 1) * 8 + (pp & 1) * 4 + (pp >> 2)) * 2;
+            }
             *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) =
                 dev::pack_f16x2(dev::bf16_lo_f32(qv[i]) * down, dev::bf16_hi_f32(qv[i]) * down);
         }
@@ -508,10 +526,18 @@ __global__ void __launch_bounds__(kThreads)
             const int c1 = tok_dim == 1 ? sub : kvh;
             const int c2 = tok_dim == 1 ? kvh : sub;
             dev::mbar_arrive_expect_tx(bar, TILE_BYTES);
-            // BF16: NBOX swizzled boxes of 64 columns; FP8: one unswizzled box of the whole row
+            // BF16: NBOX swizzled boxes of 64 columns.  FP8: K in 128-byte
+            // swizzled boxes of 128 codes (head dims from 128 up), V in one
+            // unswizzled box of the whole row.
+            if (KDIRECT && half == 0) {
 #pragma unroll
-            for (int b = 0; b < (KV8 ? 1 : NBOX); ++b)
-                dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * kBoxCols, c1, c2, id, policy);
+                for (int b = 0; b < DPAD / 128; ++b)
+                    dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * 128, c1, c2, id, policy);
+            } else {
+#pragma unroll
+                for (int b = 0; b < (KV8 ? 1 : NBOX); ++b)
+                    dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * kBoxCols, c1, c2, id, policy);
+            }
         };
 
         // Block ids of local tiles [32*win, 32*win + 64): lane l of id_cur holds
@@ -578,7 +604,7 @@ __global__ void __launch_bounds__(kThreads)
             uint8_t *stage = ring + (warp * S + k) * STAGE_BYTES;
             uint32_t kbase = dev::smem_addr(stage);
             uint32_t vbase = kbase + TILE_BYTES;
-            constexpr bool KV8_APART = KV8 && DPAD <= 128;  // K and V in f16 tiles of their own
+            constexpr bool KV8_APART = KV8 && !KDIRECT;  // K and V in f16 tiles of their own
             uint8_t *cvt = smem + plan.cvt + warp * (KV8_APART ? 2 : 1) * (kTileTokens * DPAD * 2);
             if constexpr (KV8_APART) {
                 // both halves landed -> both f16 tiles, converted back to back; the
@@ -597,14 +623,8 @@ __global__ void __launch_bounds__(kThreads)
                 }
                 kbase = dev::smem_addr(cvt);
                 vbase = kbase + kTileTokens * DPAD * 2;
-            } else if constexpr (KV8) {
-                // K: FP8 stage -> the warp's f16 tile; the stage is then free for tile r + S
-                __syncwarp();  // the previous tile's reads of the f16 tile are done
-                e4m3_tile_to_f16<DPAD>(stage, cvt, lane);
-                __syncwarp();
-                if (rn < nloc && lane == 0) issue(tmk, 0, rn, k, id_next);
-                kbase = dev::smem_addr(cvt);
-                vbase = kbase;
+            } else if constexpr (KDIRECT) {
+                vbase = dev::smem_addr(cvt);  // V is converted into the warp's f16 tile below
             }
 
             // S^T = K . q^T, two accumulator chains (even / odd k-steps)
@@ -615,21 +635,52 @@ __global__ void __launch_bounds__(kThreads)
                 for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) sc[nt][h2][c] = 0.f;
+            if constexpr (KDIRECT) {
+                // FP8 K codes straight into the A operand: per 32-code block a
+                // thread reads 8 codes of row tq and 8 of row tq + 8 (columns
+                // 32*kb + 8*qd ..), one conversion per code pair, and uses them
+                // as columns 2qd, 2qd+1 | 2qd+8, 2qd+9 of two k-steps.  q was
+                // staged in the matching column order, so the sum is the same
+                // dot product over another order of d.
+#pragma unroll(GN == 1 ? DPAD / 32 : 2)
+                for (int kb = 0; kb < DPAD / 32; ++kb) {
+                    const int qd = lane & 3;
+                    const int ch = ((kb & 3) * 2 + (qd >> 1)) ^ (tq & 7);  // swizzled 16-byte chunk
+                    const uint32_t a_lo = kbase + (kb >> 2) * (kTileTokens * 128) + tq * 128 + ch * 16 + (qd & 1) * 8;
+                    uint32_t w0x, w0y, w1x, w1y;
+                    dev::lds_v2(a_lo, w0x, w0y);
+                    dev::lds_v2(a_lo + 8 * 128, w1x, w1y);
+                    uint32_t h0[4], h1[4];
+                    dev::e4m3x4_to_f16x4(w0x, h0[0], h0[1]);
+                    dev::e4m3x4_to_f16x4(w0y, h0[2], h0[3]);
+                    dev::e4m3x4_to_f16x4(w1x, h1[0], h1[1]);
+                    dev::e4m3x4_to_f16x4(w1y, h1[2], h1[3]);
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                dev::ldsm_x4(kbase + (ks >> 2) * (kTileTokens * 128) + lmk_off[ks & 3], a0, a1, a2, a3);
+                    for (int nt = 0; nt < GN; ++nt) {
+                        uint32_t b0, b1, b2, b3;
+                        dev::ldsm_x2(q_lm + nt * 8 * QST + (2 * kb) * 32, b0, b1);
+                        dev::ldsm_x2(q_lm + nt * 8 * QST + (2 * kb + 1) * 32, b2, b3);
+                        mma_16816<true>(sc[nt][0], h0[0], h1[0], h0[1], h1[1], b0, b1);
+                        mma_16816<true>(sc[nt][1], h0[2], h1[2], h0[3], h1[3], b2, b3);
+                    }
+                }
+            } else {
 #pragma unroll
-                for (int nt = 0; nt < GN; ++nt) {
-                    uint32_t b0, b1;
-                    dev::ldsm_x2(q_lm + nt * 8 * QST + ks * 32, b0, b1);
-                    mma_16816<KV8>(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    dev::ldsm_x4(kbase + (ks >> 2) * (kTileTokens * 128) + lmk_off[ks & 3], a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < GN; ++nt) {
+                        uint32_t b0, b1;
+                        dev::ldsm_x2(q_lm + nt * 8 * QST + ks * 32, b0, b1);
+                        mma_16816<KV8>(sc[nt][ks & 1], a0, a1, a2, a3, b0, b1);
+                    }
                 }
             }
             // The K half is read (every lane's ldmatrix result has been consumed by
             // an mma): refill it with tile r + S.  A read-then-overwrite by the TMA
             // needs no proxy fence once the read values are in registers.
-            if constexpr (!KV8) {
+            if constexpr (!KV8 || KDIRECT) {
                 if (rn < nloc) {
                     __syncwarp();
                     if (lane == 0) issue(tmk, 0, rn, k, id_next);
@@ -729,7 +780,8 @@ __global__ void __launch_bounds__(kThreads)
                 }
             }
             if constexpr (KV8 && !KV8_APART) {
-                // V: FP8 stage -> the same f16 tile (q.K^T has read it)
+                // V: FP8 stage -> the warp's f16 tile (the previous tile's V^T.P^T
+                // has read it); the stage is then free for tile r + S
                 __syncwarp();
                 e4m3_tile_to_f16<DPAD>(stage + TILE_BYTES, cvt, lane);
                 __syncwarp();
