@@ -436,10 +436,15 @@ __global__ void __launch_bounds__(kThreads)
             const int g = e / (DPAD / 2);
             int d = (e - g * (DPAD / 2)) * 2;
             if constexpr (KDIRECT) {
-                // column pair P of a 32-column block sits where the direct K
-                // operand uses it: pair 4*qd + 2*h + hi -> k-step h, pair qd + 4*hi
-                const int P = d >> 1, pp = P & 15;
-                d = ((P & ~15) + ((pp >> 1) & 1) * 8 + (pp & 1) * 4 + (pp >> 2)) * 2;
+                // column pair P sits where the direct K operand uses it: in a
+                // 128-column box, chunk c (8 pairs) is read by the lanes of quad
+                // position qd = half (c even, block c/2) or 2 + half (c odd,
+                // block ((c ^ 4) - 1) / 2); its pair j goes to k-step 2*block +
+                // (j >> 1), pair qd + 4*(j & 1) of that k-step
+                const int P = d >> 1, Pb = P & 63, c = Pb >> 3, half = (Pb >> 2) & 1, j = Pb & 3;
+                const int kb = (P >> 6) * 4 + ((c & 1) ? (((c ^ 4) - 1) >> 1) : (c >> 1));
+                const int qd = (c & 1) ? 2 + half : half;
+                d = ((2 * kb + (j >> 1)) * 8 + qd + 4 * (j & 1)) * 2;
             }
             *reinterpret_cast<uint32_t *>(qsm + g * QST + d * 2) =
                 dev::pack_f16x2(dev::bf16_lo_f32(qv[i]) * down, dev::bf16_hi_f32(qv[i]) * down);
@@ -636,16 +641,20 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) sc[nt][h2][c] = 0.f;
             if constexpr (KDIRECT) {
-                // FP8 K codes straight into the A operand: per 32-code block a
-                // thread reads 8 codes of row tq and 8 of row tq + 8 (columns
-                // 32*kb + 8*qd ..), one conversion per code pair, and uses them
-                // as columns 2qd, 2qd+1 | 2qd+8, 2qd+9 of two k-steps.  q was
-                // staged in the matching column order, so the sum is the same
-                // dot product over another order of d.
+                // FP8 K codes straight into the A operand: per block kb of 32
+                // codes a thread reads 8 codes of row tq and 8 of row tq + 8
+                // (half (qd & 1) of one 16-byte chunk), one conversion per code
+                // pair, and uses them as columns 2qd, 2qd+1 | 2qd+8, 2qd+9 of
+                // k-steps 2kb and 2kb+1.  Quad positions 0-1 read chunk 2kb',
+                // 2-3 chunk (2kb'+1) ^ 4 of the box (kb' = kb mod 4): under the
+                // 128-byte swizzle the 16 lanes of each half-warp then cover the
+                // 32 banks once.  q was staged in the matching column order, so
+                // the sum is the same dot product over another order of d.
 #pragma unroll(GN == 1 ? DPAD / 32 : 2)
                 for (int kb = 0; kb < DPAD / 32; ++kb) {
                     const int qd = lane & 3;
-                    const int ch = ((kb & 3) * 2 + (qd >> 1)) ^ (tq & 7);  // swizzled 16-byte chunk
+                    const int kbp = kb & 3;
+                    const int ch = (qd < 2 ? 2 * kbp : ((2 * kbp + 1) ^ 4)) ^ (tq & 7);  // swizzled 16-byte chunk
                     const uint32_t a_lo = kbase + (kb >> 2) * (kTileTokens * 128) + tq * 128 + ch * 16 + (qd & 1) * 8;
                     uint32_t w0x, w0y, w1x, w1y;
                     dev::lds_v2(a_lo, w0x, w0y);
