@@ -39,6 +39,16 @@ def test_fp8_shapes_and_splits(cuda_device, Hq, Hkv, D, N):
     assert np.all(got[0] == 0.0)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 80), (12, 4, 96), (8, 1, 112), (8, 2, 160), (16, 4, 208)])
+@pytest.mark.parametrize("N", [1, 4])
+def test_fp8_head_dims_below_the_padded_width(cuda_device, Hq, Hkv, D, N):
+    # K is read in boxes of 128 codes that reach past head_dim (zero-filled
+    # there, with q zero in the same columns); V in one box of the padded row
+    lens = [1, 16, 33, 600, 1500]
+    w = W.fp8_variant(W.custom(lens, Hq, Hkv, D, seed=190 + D), k_scale=0.6, v_scale=1.3, seed=D + 1)
+    assert_within_tolerance(_run(w, cuda_device, N), _ref(w), f"fp8 Hq{Hq} Hkv{Hkv} D{D} N{N}")
+
+
 @pytest.mark.parametrize("pack,N", [(1, 1), (2, 4)])
 def test_fp8_packed(cuda_device, pack, N):
     w = W.fp8_variant(W.custom([0, 33, 512, 4000], 16, 2, 256, seed=95), seed=5)
