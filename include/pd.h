@@ -5,7 +5,8 @@
  *
  *     out[s,h,:] = softmax(q[s,h,:] . K[s,kvh,:,:]^T * inv_sqrt_d) . V[s,kvh,:,:]
  *
- * over a BF16 KV cache paged in blocks, with grouped-query sharing
+ * over a BF16 KV cache paged in blocks (or one of FP8 E4M3 codes with
+ * per-tensor scales, pd_decode_attn_fp8), with grouped-query sharing
  * (kvh = h / (num_q_heads / num_kv_heads)), and writes BF16; a sequence with
  * no token gets 0.  Sources: the "Module attn_splitk" documentation page
  * (split-K launch geometry, the split-K workspace of [o, m, l] slots, the
