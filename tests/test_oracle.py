@@ -484,7 +484,10 @@ def _mutant_lib(name, tmpdir):
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_planted_mistake_is_caught(name, monkeypatch):
-    tmp = tempfile.mkdtemp()
+    # scratch beside the oracle's own build (an ignored build folder of the repository)
+    scratch = os.path.join(os.path.dirname(oracle.__file__), "_build")
+    os.makedirs(scratch, exist_ok=True)
+    tmp = tempfile.mkdtemp(dir=scratch)
     try:
         lib = _mutant_lib(name, tmp)
         real = oracle._load()
