@@ -5,7 +5,8 @@ Covers the five workloads at full size (the large-batch one on sampled
 sequences, since the oracle is slow there), every split count on the tiny
 workload, ragged and edge-case shapes (empty sequences, 1-token sequences,
 partial last tiles, head dims that are not multiples of 64, group widths from
-1 to 32, block sizes 16/32/64) and both tiled layouts."""
+1 to 32, block sizes 16/32/64/256, 4096 short sequences, 32 single-head groups
+at head dim 256) and both tiled layouts."""
 
 import numpy as np
 import pytest
@@ -61,6 +62,24 @@ EDGE_SHAPES = [
     ([70000], 8, 1, 64, 16, 16),                 # one very long sequence at 16 splits
     ([300, 9, 2600], 32, 2, 128, 16, 3),         # group 16 at head dim 128
 ]
+
+
+@pytest.mark.parametrize("N", [1, 4])
+def test_many_short_sequences(cuda_device, N):
+    # 4096 sequences of 1..64 tokens: a grid of many waves of one-CTA units and,
+    # at N = 4, a merge over 32768 rows (most sequences use one split)
+    lens = np.random.default_rng(77).integers(1, 65, size=4096).tolist()
+    w = W.custom(lens, 8, 2, 128, seed=78)
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    assert_within_tolerance(_run(w, cuda_device, num_splits=N, gqa_pack=False), ref, f"4096 short N={N}")
+
+
+def test_wide_multi_head_at_head_dim_256(cuda_device):
+    # group 1 at the largest head dim: 32 KV heads, one query head each
+    w = W.custom([1, 300, 2500], 32, 32, 256, seed=79)
+    ref = oracle.decode_attn(w.q, w.k_cache, w.v_cache, w.block_table, w.context_lens, w.inv_sqrt_d)
+    for n in (1, 3):
+        assert_within_tolerance(_run(w, cuda_device, num_splits=n, gqa_pack=False), ref, f"MHA D256 N={n}")
 
 
 @pytest.mark.parametrize("lens,Hq,Hkv,D,bs,N", EDGE_SHAPES)
