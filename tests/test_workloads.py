@@ -1,0 +1,71 @@
+"""The synthetic inputs are the recipe the measurements are quoted on: each
+workload's shape, policy and algorithmic K/V bytes (seed 0), and the
+structure of its placement (every sequence's blocks distinct and inside a pool
+of ceil(1.25 x needed) blocks).  CPU only; the large batch is checked through
+its length generator, without drawing its 3 GB of values."""
+
+import numpy as np
+import pytest
+
+from oracle import policy as P
+from paged_kv_decode_splitk_gb300 import workloads as W
+
+
+def _placement_ok(w):
+    need = -(-w.context_lens.astype(np.int64) // w.block_size)
+    used = np.concatenate([w.block_table[s, :n] for s, n in enumerate(need)] or [np.zeros(0, np.int32)])
+    assert len(np.unique(used)) == len(used), "a block serves two places"
+    assert used.min(initial=0) >= 0 and used.max(initial=0) < w.num_blocks
+
+
+def test_tiny():
+    w = W.tiny()
+    assert (w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks) == (4, 1, 64, 16, 16)
+    assert w.context_lens.tolist() == [37, 100] and w.inv_sqrt_d == 0.125
+    assert w.kv_bytes == 35_072
+    _placement_ok(w)
+
+
+def test_gqa_packed():
+    w = W.gqa_packed()
+    assert (w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size) == (32, 16, 2, 256, 16)
+    assert w.context_lens.min() >= 512 and w.context_lens.max() <= 4096
+    assert w.gqa_pack and P.gqa_pack_shape_ok(16, 2, 256)
+    assert w.kv_bytes == 150_677_504
+    need = int((-(-w.context_lens.astype(np.int64) // 16)).sum())
+    assert w.num_blocks == int(np.ceil(1.25 * need))
+    _placement_ok(w)
+
+
+def test_long_context():
+    w = W.long_context()
+    assert (w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim) == (1, 24, 8, 128)
+    assert w.kv_bytes == 32768 * 8 * 128 * 2 * 2 == 134_217_728
+    assert P.num_splits(P.POLICY_AUTO, 0, w.sm_count, w.num_q_heads, 1, 0) == 13
+
+
+def test_large_batch_lengths():
+    lens = W.large_batch_lens()
+    assert lens.size == 256 and lens.min() >= 16 and lens.max() <= 16384
+    assert abs(float(np.median(lens)) - 2048) < 400
+    assert int(lens.sum()) * 8 * 128 * 2 * 2 == 3_174_469_632
+    assert P.num_splits(P.POLICY_AUTO, 0, 148, 32, 256, 0) == 10
+
+
+def test_tiled():
+    tw = W.tiled()
+    assert (tw.num_seqs, tw.num_q_heads, tw.num_kv_heads, tw.head_dim, tw.block_size) == (64, 16, 4, 256, 16)
+    assert tw.tile_capacity == 64 and tw.num_calls == 4 and tw.layout == "scratch"
+    assert tw.kv_bytes == 510_287_872
+    assert int((tw.blocks_per_seq == 0).sum()) >= 2
+    # right-aligned calls: full blocks before the last call, 5 valid slots in it
+    assert list(tw.last_block_valid_slots[:-1]) == [16] * 3 and tw.last_block_valid_slots[-1] == 5
+
+
+def test_fp8_variant_halves_the_bytes():
+    w = W.fp8_variant(W.custom([100, 700], 8, 2, 128, seed=3), k_scale=0.5, v_scale=0.25, seed=4)
+    assert w.kv_dtype == "e4m3" and w.k_cache.dtype == np.uint8 and w.kv_elem_bytes == 1
+    bf = W.custom([100, 700], 8, 2, 128, seed=3)
+    assert 2 * w.kv_bytes == bf.kv_bytes
+    # no NaN code (0x7f / 0xff) in the cache
+    assert not np.any((w.k_cache & 0x7F) == 0x7F) and not np.any((w.v_cache & 0x7F) == 0x7F)
