@@ -243,16 +243,21 @@ int pd_decode_attn_fp8(const void *q, const void *k_cache, const void *v_cache, 
  *
  * Arguments, shapes, results and error codes are those of pd_decode_attn
  * without workspace / workspace_bytes: the split-K workspace is a fixed
- * PD_NOALLOC_WORKSPACE_BYTES array that libpd holds in every GPU's memory
- * from the moment the library's kernels are loaded on it until the process
- * exits.  A launch whose workspace (pd_workspace_bytes(num_seqs, num_q_heads,
- * head_dim, num_splits), 0 when num_splits == 1) would exceed that size is
- * rejected with PD_ERR_WORKSPACE and launches nothing.  Nothing is allocated,
- * by this call or by anything it calls.
+ * PD_NOALLOC_WORKSPACE_BYTES array in libpd's device code, which a GPU holds
+ * from the moment that code is loaded on it until the process exits.  A
+ * launch whose workspace (pd_workspace_bytes(num_seqs, num_q_heads, head_dim,
+ * num_splits), 0 when num_splits == 1) would exceed that size is rejected
+ * with PD_ERR_WORKSPACE and launches nothing.  The call itself allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *
- * The first call on a device looks up that device's address of the array
- * (cudaGetSymbolAddress, with the device current); make that first call
- * before any stream capture.  All calls on a device share the one array and
+ * Set-up: the first call with num_splits > 1 on a device looks up that
+ * device's address of the array (cudaGetSymbolAddress, with the device
+ * current).  Under the CUDA driver's lazy module loading (the default since
+ * CUDA 12) that lookup is also what loads the array into the device's memory,
+ * so the 16 MiB are taken then, not when the library is opened.  Make that
+ * first call at start-up, while the memory is still free and before any
+ * stream capture; later calls only read the cached address.  All calls on a
+ * device share the one array and
  * it keeps the previous call's contents; no part of it needs to start at zero
  * (every value a call reads is written earlier in the same call), but two
  * calls whose kernels overlap on the GPU, on different streams or from
@@ -289,9 +294,12 @@ int pd_tiled_validate(const pd_tiled_dims *dims);
 int pd_tiled_state_bytes(const pd_tiled_dims *dims, size_t *m_bytes, size_t *l_bytes,
                          size_t *o_bytes, size_t *output_bytes);
 
-/* TiledAttention::new: validate and allocate the FP32 running state (m, l, o)
- * once, on the current device.  *out receives the handle.  Returns PD_OK,
- * PD_ERR_INVALID, PD_ERR_UNSUPPORTED, PD_ERR_ALLOC or PD_ERR_CUDA. */
+/* TiledAttention::new: validate and allocate, once, on the current device, the
+ * FP32 running state (m, l, o) and the buffer pd_tiled_run keeps the per-call
+ * partials of one step in (max_seqs * num_q_heads * 8 * (head_dim + 2)
+ * floats: one [o, m, l] slot per row for each of up to 8 calls), so that no
+ * later call on the handle allocates.  *out receives the handle.  Returns
+ * PD_OK, PD_ERR_INVALID, PD_ERR_UNSUPPORTED, PD_ERR_ALLOC or PD_ERR_CUDA. */
 int pd_tiled_create(const pd_tiled_dims *dims, pd_tiled **out);
 
 /* Free the state (NULL is a no-op).  Synchronises the device first. */
@@ -362,12 +370,11 @@ typedef struct pd_tiled_source {
  * the running state and `out` untouched.  The result equals one begin, the
  * steps and one finalize made separately (same kernels, same order).
  * num_sources may be 0 (out = 0).  With 1..8 sources the step runs as two
- * launches (every call's tile at once, then the in-order fold and finalize)
- * instead of 2 + num_sources; the first such run on a handle allocates the
- * handle's partials buffer (max_seqs * num_q_heads * 8 * (head_dim + 2)
- * floats), so it must not be the first call inside a CUDA graph capture.
- * Returns PD_OK, PD_ERR_CAPACITY, PD_ERR_INVALID, PD_ERR_ALLOC or
- * PD_ERR_CUDA. */
+ * launches (every call's tile at once, writing each call's partial to the
+ * handle's partials buffer, then the in-order fold and finalize) instead of
+ * 2 + num_sources.  Nothing is allocated: any call, the first included, may
+ * be captured in a CUDA graph.
+ * Returns PD_OK, PD_ERR_CAPACITY, PD_ERR_INVALID or PD_ERR_CUDA. */
 int pd_tiled_run(pd_tiled *t, const void *q, const pd_tiled_source *sources, int num_sources,
                  void *out, int num_seqs, void *stream);
 
@@ -378,11 +385,17 @@ int pd_tiled_run(pd_tiled *t, const void *q, const pd_tiled_source *sources, int
  * Returns PD_OK or PD_ERR_CUDA. */
 int pd_device_status(int *flags);
 
-/* Test hook: make the next `count` state allocations in pd_tiled_create fail
- * as if the device were out of memory (host-side fault injection). */
+/* ---- test hooks ----
+ * Not part of the decode interface: the test suite and launch-shape
+ * experiments use them.  A program that serves decode steps never needs to
+ * call either. */
+
+/* TEST HOOK.  Make the next `count` device allocations of pd_tiled_create
+ * (state m, l, o, then the run partials) fail as if the device were out of
+ * memory (host-side fault injection). */
 void pd_debug_fail_next_allocs(int count);
 
-/* Tuning hook for launch-shape experiments, applied to the following launches
+/* TEST HOOK.  Tuning for launch-shape experiments, applied to the following launches
  * in this process: pipeline stages per warp (1..8; 0 = built-in), where the
  * parts of a unit run (0 = chosen from occupancy, 1 = one CTA per unit, > 1 =
  * one CTA per part in a thread-block cluster) and longest-first service order

@@ -280,17 +280,18 @@ def pd_decode_attn_fp8(q, k_cache, v_cache, k_scale: float, v_scale: float, bloc
 
 
 def pd_decode_attn_noalloc(q, k_cache, v_cache, block_table, context_lens, out, inv_sqrt_d: float,
-                           num_splits: int, gqa_pack: bool = False, stream=None,
+                           num_splits: int, gqa_pack: int = 0, stream=None,
                            num_blocks: int | None = None) -> int:
     """pd_decode_attn with the split-K workspace held by the library (see pd.h): for
-    callers that cannot allocate device memory.  Same tensors and shapes, no workspace."""
+    callers that cannot allocate device memory.  Same tensors, shapes and gqa_pack
+    modes (0 off, 1 packed non-split, 2 packed with splits), no workspace."""
     S, Hq, D = q.shape
     nb, bs, Hkv, D2 = k_cache.shape
     assert D2 == D, "head_dim mismatch"
     rc = lib().pd_decode_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                       int(block_table.shape[1]), _ptr(context_lens), _ptr(out), S, Hq,
                                       Hkv, D, bs, nb if num_blocks is None else num_blocks,
-                                      float(inv_sqrt_d), int(num_splits), int(bool(gqa_pack)),
+                                      float(inv_sqrt_d), int(num_splits), int(gqa_pack),
                                       _stream(stream))
     return _check(rc)
 
