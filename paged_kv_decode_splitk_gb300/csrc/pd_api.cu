@@ -327,8 +327,17 @@ struct pd_tiled {
     float *l;
     float *o;
     int device;
-    float *run_ws;  // per-call partials of a fused pd_tiled_run, allocated on its first use
+    float *run_ws;  // per-call partials of a fused pd_tiled_run [max_seqs*Hq, kMaxRunSources, D + 2]
 };
+
+namespace {
+// Floats of a handle's fused-run partials: one [o[D], m, l] slot per (row, call)
+// for up to kMaxRunSources calls.
+size_t run_partials_floats(const pd_tiled_dims &d) {
+    return static_cast<size_t>(d.max_seqs) * d.num_q_heads * pd::kMaxRunSources *
+           (static_cast<size_t>(d.head_dim) + 2);
+}
+}  // namespace
 
 namespace {
 std::atomic<int> g_fail_allocs{0};
@@ -696,9 +705,9 @@ int pd_tiled_create(const pd_tiled_dims *dims, pd_tiled **out) {
     pd_tiled *t = new pd_tiled();
     t->dims = *dims;
     t->device = dev;
-    float **bufs[3] = {&t->m, &t->l, &t->o};
-    size_t sizes[3] = {mb, lb, ob};
-    for (int i = 0; i < 3; ++i) {
+    float **bufs[4] = {&t->m, &t->l, &t->o, &t->run_ws};
+    size_t sizes[4] = {mb, lb, ob, run_partials_floats(*dims) * sizeof(float)};
+    for (int i = 0; i < 4; ++i) {
         void *p = nullptr;
         int inject = g_fail_allocs.load();
         while (inject > 0 && !g_fail_allocs.compare_exchange_weak(inject, inject - 1)) {
@@ -712,6 +721,7 @@ int pd_tiled_create(const pd_tiled_dims *dims, pd_tiled **out) {
             cudaFree(t->m);
             cudaFree(t->l);
             cudaFree(t->o);
+            cudaFree(t->run_ws);
             delete t;
             return fail(PD_ERR_ALLOC, "tiled state allocation of %zu bytes failed: %s", sizes[i],
                         cudaGetErrorString(e));
@@ -904,26 +914,12 @@ namespace {
 // every (sequence, KV head, call) writes one partial [o, m, l] per call, and
 // the fold pass replays step_tile's fold of those partials in call order from
 // begin's (-inf, 0, 0), then finalizes.  Same arithmetic, same bits, as the
-// calls made one by one.  The partials live in a buffer of the handle,
-// allocated on the first fused run (kMaxRunSources slots per row).
+// calls made one by one.  The partials live in the buffer pd_tiled_create
+// allocated with the state (kMaxRunSources slots per row), so a run allocates
+// nothing.
 int tiled_run_fused(pd_tiled *t, const void *q, const pd_tiled_source *sources, int num_sources, void *out,
                     int num_seqs, void *stream) {
     const pd_tiled_dims &d = t->dims;
-    if (!t->run_ws) {
-        const size_t n = static_cast<size_t>(d.max_seqs) * d.num_q_heads * pd::kMaxRunSources *
-                         (static_cast<size_t>(d.head_dim) + 2);
-        int inject = g_fail_allocs.load();
-        while (inject > 0 && !g_fail_allocs.compare_exchange_weak(inject, inject - 1)) {
-        }
-        if (inject > 0) return fail(PD_ERR_ALLOC, "fused tiled run: partials buffer (injected failure)");
-        void *ptr = nullptr;
-        cudaError_t ae = cudaMalloc(&ptr, n * sizeof(float));
-        if (ae != cudaSuccess) {
-            cudaGetLastError();
-            return fail(PD_ERR_ALLOC, "fused tiled run: cannot allocate %zu bytes of partials", n * sizeof(float));
-        }
-        t->run_ws = static_cast<float *>(ptr);
-    }
     const int G = d.num_q_heads / d.num_kv_heads;
     const int dpad = dpad_for(d.head_dim);
     const int gn = G <= 8 ? 1 : 2;

@@ -162,23 +162,37 @@ def test_tiled_run_checks_every_source_before_launching(cuda_device):
         t.close()
 
 
-def test_fused_tiled_run_reports_allocation_failure(cuda_device):
-    """The first fused pd_tiled_run allocates the handle's partials buffer: an
-    injected failure is reported as PD_ERR_ALLOC, and the next run succeeds."""
+def test_fused_tiled_run_on_a_fresh_handle_is_capturable(cuda_device):
+    """pd_tiled_create allocates the fused run's partials with the state, so the
+    first pd_tiled_run on a handle allocates nothing and can be the first call
+    inside a CUDA graph capture; the replay equals the calls made one by one
+    on another handle."""
     mw = W.tiled_mixed(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_dim=64, tile_capacity=8,
                        max_blocks=16, seed=58)
     inp = api.MixedTiledInputs(mw, cuda_device)
-    t = pd.Tiled(3, 8, 2, 64, 16, 8)
+    ref_t = pd.Tiled(3, 8, 2, 64, 16, 8)
+    t = None
     try:
-        out = torch.empty((3, 8, 64), dtype=torch.bfloat16, device=cuda_device)
-        pd.pd_debug_fail_next_allocs(1)
-        with pytest.raises(pd.PdError) as e:
-            t.run(inp.q, inp.sources(t), out, 3)
-        assert e.value.code == pd.PD_ERR_ALLOC
-        pd.pd_debug_fail_next_allocs(0)
-        t.run(inp.q, inp.sources(t), out, 3)
+        # the calls one by one on one handle (this also loads the kernels)
+        ref = torch.empty((3, 8, 64), dtype=torch.bfloat16, device=cuda_device)
+        ref_t.begin(3)
+        for k, v, tb, tc, st, lb in inp.sources(ref_t):
+            ref_t.step(inp.q, k, v, tb, tc, 3, st, lb)
+        ref_t.finalize(ref, 3)
+        torch.cuda.synchronize()
+        # a fresh handle whose first call is the captured run
+        t = pd.Tiled(3, 8, 2, 64, 16, 8)
+        out = torch.full((3, 8, 64), 7.0, dtype=torch.bfloat16, device=cuda_device)
+        srcs = inp.sources(t)
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            t.run(inp.q, srcs, out, 3)
+        g.replay()
         torch.cuda.synchronize()
         assert pd.pd_device_status() == 0
+        assert np.array_equal(api.bf16_bits(out), api.bf16_bits(ref))
     finally:
-        pd.pd_debug_fail_next_allocs(0)
-        t.close()
+        ref_t.close()
+        if t is not None:
+            t.close()
