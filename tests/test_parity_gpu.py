@@ -1,8 +1,8 @@
 """GPU parity: libpd (through the C ABI) against the FP64 oracle, element by
 element, within |gpu - ref| <= ulp_bf16(ref) + 1e-3.
 
-Covers the five workloads at full size (the large-batch one on sampled
-sequences, since the oracle is slow there), every split count on the tiny
+Covers the five workloads at full size (whole outputs; the large-batch
+reference is computed on every host core), every split count on the tiny
 workload, ragged and edge-case shapes (empty sequences, 1-token sequences,
 partial last tiles, head dims that are not multiples of 64, group widths from
 1 to 32, block sizes 16/32/64/256, 4096 short sequences, 32 single-head groups
@@ -16,7 +16,7 @@ from oracle import policy as P
 from paged_kv_decode_splitk_gb300 import api, pd
 from paged_kv_decode_splitk_gb300 import workloads as W
 
-from helpers import assert_within_tolerance, oracle_rows
+from helpers import assert_within_tolerance, oracle_all_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -127,17 +127,14 @@ def test_long_context_full_size(cuda_device):
     assert_within_tolerance(_run(w, cuda_device, num_splits=n), ref, "long_context")
 
 
-def test_large_batch_full_size_sampled(cuda_device):
+def test_large_batch_full_size_whole_output(cuda_device):
+    """All 256 x 32 x 128 outputs of the large-batch step (10 splits, several
+    waves, longest-first order off) against the oracle, element by element."""
     w = W.large_batch()
     n = pd.pd_num_splits("auto", 0, 148, w.num_q_heads, w.num_seqs, 0)
     assert n == 10
     got = _run(w, cuda_device, num_splits=n)
-    lens = w.context_lens
-    rng = np.random.default_rng(7)
-    pick = sorted(set([int(np.argmax(lens)), int(np.argmin(lens)), 0, w.num_seqs - 1]
-                      + list(rng.choice(w.num_seqs, 8, replace=False))))
-    ref = oracle_rows(w, pick)
-    assert_within_tolerance(got[pick], ref, "large_batch sample")
+    assert_within_tolerance(got, oracle_all_rows(w), "large_batch whole output")
 
 
 def _tiled_check(tw, device, what):
@@ -248,3 +245,16 @@ def test_gqa_packed_splitk_shape_gate(cuda_device):
         pd.pd_decode_attn(inp.q, inp.k, inp.v, inp.block_table, inp.context_lens, out, w.inv_sqrt_d,
                           1, None, 3)
     assert e.value.code == pd.PD_ERR_INVALID
+
+
+@pytest.mark.parametrize("name", ["gqa_packed_long", "gqa_packed_long_splitk"])
+def test_gqa_packed_long_full_size(cuda_device, name):
+    """Few long sequences at the packed shape (2 x 32768 tokens, Hq 16, Hkv 2,
+    D 256), through the non-split packed pass and through the packed pass with
+    Auto's 16 splits, on the same inputs."""
+    w = W.WORKLOADS[name]()
+    inp = api.PagedInputs(w, cuda_device)
+    n = inp.splits()
+    assert n == (16 if w.gqa_pack == 2 else 1)
+    ref = oracle_all_rows(w)
+    assert_within_tolerance(_run(w, cuda_device, num_splits=n, gqa_pack=w.gqa_pack), ref, name)
