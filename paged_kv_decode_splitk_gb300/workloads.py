@@ -144,6 +144,26 @@ def gqa_packed_splitk(seed: int = SEED_VALUES) -> PagedWorkload:
                   policy="auto", sm_count=148, gqa_pack=2)
 
 
+def _packed_long_lens() -> list:
+    return [32768, 32768]
+
+
+def gqa_packed_long(seed: int = SEED_VALUES) -> PagedWorkload:
+    """Few long sequences at the packed shape: 2 sequences of 32768 tokens; Hq 16,
+    Hkv 2 (pack width 8), D 256, block 16; non-split launch through the packed
+    pass (only 2 x 2 = 4 units)."""
+    return _paged("gqa_packed_long_2x32768_h16kv2_d256", _packed_long_lens(), 16, 2, 256, 16, seed + 400,
+                  policy="pinned", pin=1, gqa_pack=True)
+
+
+def gqa_packed_long_splitk(seed: int = SEED_VALUES) -> PagedWorkload:
+    """The same sequences, cache and block table through the packed pass with
+    splits (gqa_pack mode 2) at Auto: ceil(296 / 16) = 19, clamped to 16 splits
+    of 2048 tokens each."""
+    return _paged("gqa_packed_long_splitk_2x32768_h16kv2_d256", _packed_long_lens(), 16, 2, 256, 16,
+                  seed + 400, policy="auto", sm_count=148, gqa_pack=2)
+
+
 def long_context(seed: int = SEED_VALUES) -> PagedWorkload:
     """1 sequence of 32768 tokens; Hq 24, Hkv 8, D 128, block 16; Auto at 148 SMs (13 splits)."""
     return _paged("long_context_1x32768_h24kv8_d128", [32768], 24, 8, 128, 16, seed + 200,
@@ -444,6 +464,8 @@ WORKLOADS = {
     "tiny": tiny,
     "gqa_packed": gqa_packed,
     "gqa_packed_splitk": gqa_packed_splitk,
+    "gqa_packed_long": gqa_packed_long,
+    "gqa_packed_long_splitk": gqa_packed_long_splitk,
     "gqa_packed_fp8": gqa_packed_fp8,
     "long_context_fp8": long_context_fp8,
     "large_batch_fp8": large_batch_fp8,

@@ -206,3 +206,14 @@ def test_packed_with_splits_is_batch_invariant(cuda_device):
         alone = _bits(_sub_batch(w, [s], relocate_seed=s + 1), cuda_device, 16, pack=2)
         assert np.array_equal(alone[0], full[s])
     assert np.array_equal(_bits(w, cuda_device, 1, pack=2), _bits(w, cuda_device, 1, pack=1))
+
+
+def test_packed_long_sequence_with_splits_alone_vs_pair(cuda_device):
+    """gqa_pack mode 2 at Auto's 16 splits: each 32768-token sequence of the
+    long packed workload gives the same bits alone as next to the other one."""
+    w = W.gqa_packed_long_splitk()
+    n = api.PagedInputs(w, cuda_device).splits()
+    both = _bits(w, cuda_device, n, pack=2)
+    for s in range(w.num_seqs):
+        alone = _bits(_sub_batch(w, [s], relocate_seed=40 + s), cuda_device, n, pack=2)
+        assert np.array_equal(alone[0], both[s])

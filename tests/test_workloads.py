@@ -69,3 +69,18 @@ def test_fp8_variant_halves_the_bytes():
     assert 2 * w.kv_bytes == bf.kv_bytes
     # no NaN code (0x7f / 0xff) in the cache
     assert not np.any((w.k_cache & 0x7F) == 0x7F) and not np.any((w.v_cache & 0x7F) == 0x7F)
+
+
+def test_gqa_packed_long_pair():
+    """Few long sequences at the packed shape: the non-split and the split
+    variant draw the same sequences, cache and block table."""
+    a, b = W.gqa_packed_long(), W.gqa_packed_long_splitk()
+    for w in (a, b):
+        assert (w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size) == (2, 16, 2, 256, 16)
+        assert w.context_lens.tolist() == [32768, 32768]
+        assert w.kv_bytes == 2 * 32768 * 2 * 256 * 2 * 2 == 134_217_728
+        _placement_ok(w)
+    assert a.gqa_pack == 1 and a.policy == "pinned" and a.pin == 1
+    assert b.gqa_pack == 2 and P.num_splits(P.POLICY_AUTO, 0, b.sm_count, b.num_q_heads, 2, 0) == 16
+    assert np.array_equal(a.k_cache, b.k_cache) and np.array_equal(a.block_table, b.block_table)
+    assert np.array_equal(a.q, b.q)
