@@ -390,9 +390,9 @@ def run_ours(args):
     # so that the clock samples taken meanwhile describe the clocks it ran at.
     soak_reps = max(1, int(1000.0 / ms_multi))
     soak_s = soak_reps * ms_multi / 1e3
-    for _ in range(soak_reps):
-        g_multi.replay()
     with ClockSampler(local) as clk:
+        for _ in range(soak_reps):
+            g_multi.replay()
         evs[0].record(stream)
         for j in range(n_multi):
             g_multi.replay()

@@ -571,16 +571,17 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     const long long kvh_s = head_dim, tok_s = static_cast<long long>(num_kv_heads) * head_dim;
     const long long blk_s = tok_s * block_size;
     const int elem = kv8 ? 1 : 2;
-    // FP8 from head dim 128 up: K in 128-code swizzled boxes (read straight into
-    // the mma operands), V in one unswizzled box of the padded row
+    // FP8 from head dim 128 up: K and V in 128-code swizzled boxes (read
+    // straight into the mma operands); at head dim 64 one unswizzled box of the
+    // padded row each (converted to f16 tiles first)
     const bool k_direct = kv8 && dpad >= 128;
     const int box_k = !kv8 ? pd::kBoxCols : (k_direct ? 128 : dpad);
-    const int box_v = kv8 ? dpad : pd::kBoxCols;
+    const int box_v = box_k;
     rc = encode_kv_map(&tk, &tok_dim, k_cache, head_dim, block_size, num_kv_heads, num_blocks, blk_s,
                        tok_s, kvh_s, elem, box_k, !kv8 || k_direct);
     if (rc != PD_OK) return rc;
     rc = encode_kv_map(&tv, &tok_dim, v_cache, head_dim, block_size, num_kv_heads, num_blocks, blk_s,
-                       tok_s, kvh_s, elem, box_v, !kv8);
+                       tok_s, kvh_s, elem, box_v, !kv8 || k_direct);
     if (rc != PD_OK) return rc;
 
     pd::UnitParams p = {};

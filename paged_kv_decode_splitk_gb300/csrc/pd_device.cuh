@@ -145,6 +145,21 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, 
                  : "memory");
 }
 
+__device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// Byte permute: byte i of the result is byte ((sel >> 4i) & 7) of the eight
+// bytes {b, a} (a holds bytes 0-3, b bytes 4-7).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
 __device__ __forceinline__ void lds_v2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
 }

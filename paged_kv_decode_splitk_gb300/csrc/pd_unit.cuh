@@ -26,10 +26,10 @@
 //     barrier when every rank holds a part.
 //   * K and V tiles move global -> shared with 4-D TMA tensor loads gathered
 //     through the block table (BF16: one 128-byte-swizzled box per 64
-//     columns; FP8 E4M3 from head dim 128 up: K in 128-byte-swizzled boxes of
-//     128 codes whose codes each thread converts straight into its mma
-//     operands, V in one box of the padded row converted by the warp to an
-//     f16 tile in the BF16 layout; at head dim 64 both go through f16 tiles).
+//     columns; FP8 E4M3 from head dim 128 up: K and V in 128-byte-swizzled
+//     boxes of 128 codes whose codes each thread converts straight into its
+//     mma operands, V's pairs of tokens gathered by byte permutes; at head dim
+//     64 both go through f16 tiles converted by the warp).
 //     Each warp runs a private ring
 //     of `stages` buffers with separate K and V mbarriers, refilled as soon
 //     as their data has been read, so the next tiles' loads overlap the
@@ -104,9 +104,9 @@ __host__ __device__ inline UnitSmem unit_smem_plan(int dpad, int rows, int stage
     const int result = rows * ostride * 4;
     s.stages = 0;
     s.cvt = (ring + 1023) / 1024 * 1024;
-    // f16 tiles per warp: K and V apart at head dims up to 64; from 128 up only
-    // V is converted (K's codes go straight into the mma operands)
-    const int cvt_tiles = dpad <= 64 ? 2 : 1;
+    // f16 tiles per warp: K and V apart at head dims up to 64; from 128 up none
+    // (both operands are built in registers from the landed codes)
+    const int cvt_tiles = dpad <= 64 ? 2 : 0;
     const int loop_end = kv8 ? s.cvt + kWarps * cvt_tiles * kTileTokens * dpad * 2 : ring;
     s.merge = 0;
     s.result = merge;
@@ -165,15 +165,20 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         dev::mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
 }
 
-template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8>
-__global__ void __launch_bounds__(kThreads)
+// CAP4: the same kernel held to 128 registers (4 CTAs per SM; no spill over an
+// FP8 cache at head dim 128 with groups of up to 4 rows), for launches of
+// many waves of short CTAs, where more resident CTAs hide more of each CTA's
+// start and end.  Otherwise the compiler chooses (a bound of 0 blocks).
+template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8, bool CAP4 = false>
+__global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     unit_kernel(const __grid_constant__ KvMaps<MODE == kModeTiledRun ? kMaxRunSources : 1> maps,
                 const __grid_constant__ UnitParams p) {
     constexpr int KS = DPAD / 16;      // mma k-steps of K.q^T == m-tiles of V^T.P^T
     constexpr int NBOX = DPAD / kBoxCols;                 // BF16 boxes per tile (64 columns each)
-    // FP8 cache from head dim 128 up: K's codes go from the (128-byte swizzled)
-    // FP8 tile straight into the mma operands; only V passes through an f16 tile.
+    // FP8 cache from head dim 128 up: K's and V's codes go from the (128-byte
+    // swizzled) FP8 tiles straight into the mma operands.
     constexpr bool KDIRECT = KV8 && DPAD >= 128;
+    constexpr bool VDIRECT = KDIRECT;
     constexpr int TILE_BYTES = kTileTokens * DPAD * (KV8 ? 1 : 2);  // one landed K or V tile
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static_assert(!KV8 || MODE == kModePaged, "FP8 caches are a paged-mode source");
@@ -312,14 +317,18 @@ __global__ void __launch_bounds__(kThreads)
                         const int sub = (gt % tiles_per_block) * kTileTokens;
                         const int c1 = tok_dim == 1 ? sub : kvh;
                         const int c2 = tok_dim == 1 ? kvh : sub;
-#pragma unroll
-                        for (int b = 0; b < (KV8 ? 1 : NBOX); ++b) {
-                            dev::tma_prefetch_4d(tmv, b * kBoxCols, c1, c2, id);
-                            if constexpr (!KDIRECT) dev::tma_prefetch_4d(tmk, b * kBoxCols, c1, c2, id);
-                        }
                         if constexpr (KDIRECT) {
 #pragma unroll
-                            for (int b = 0; b < DPAD / 128; ++b) dev::tma_prefetch_4d(tmk, b * 128, c1, c2, id);
+                            for (int b = 0; b < DPAD / 128; ++b) {
+                                dev::tma_prefetch_4d(tmk, b * 128, c1, c2, id);
+                                dev::tma_prefetch_4d(tmv, b * 128, c1, c2, id);
+                            }
+                        } else {
+#pragma unroll
+                            for (int b = 0; b < (KV8 ? 1 : NBOX); ++b) {
+                                dev::tma_prefetch_4d(tmv, b * kBoxCols, c1, c2, id);
+                                dev::tma_prefetch_4d(tmk, b * kBoxCols, c1, c2, id);
+                            }
                         }
                     }
                 }
@@ -531,10 +540,10 @@ __global__ void __launch_bounds__(kThreads)
             const int c1 = tok_dim == 1 ? sub : kvh;
             const int c2 = tok_dim == 1 ? kvh : sub;
             dev::mbar_arrive_expect_tx(bar, TILE_BYTES);
-            // BF16: NBOX swizzled boxes of 64 columns.  FP8: K in 128-byte
-            // swizzled boxes of 128 codes (head dims from 128 up), V in one
+            // BF16: NBOX swizzled boxes of 64 columns.  FP8 from head dim 128
+            // up: 128-byte swizzled boxes of 128 codes; at head dim 64 one
             // unswizzled box of the whole row.
-            if (KDIRECT && half == 0) {
+            if (KDIRECT) {
 #pragma unroll
                 for (int b = 0; b < DPAD / 128; ++b)
                     dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * 128, c1, c2, id, policy);
@@ -610,8 +619,8 @@ __global__ void __launch_bounds__(kThreads)
             uint32_t kbase = dev::smem_addr(stage);
             uint32_t vbase = kbase + TILE_BYTES;
             constexpr bool KV8_APART = KV8 && !KDIRECT;  // K and V in f16 tiles of their own
-            uint8_t *cvt = smem + plan.cvt + warp * (KV8_APART ? 2 : 1) * (kTileTokens * DPAD * 2);
             if constexpr (KV8_APART) {
+                uint8_t *cvt = smem + plan.cvt + warp * 2 * (kTileTokens * DPAD * 2);
                 // both halves landed -> both f16 tiles, converted back to back; the
                 // stage is then free for tile r + S
                 if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 1]), par)) {
@@ -628,8 +637,6 @@ __global__ void __launch_bounds__(kThreads)
                 }
                 kbase = dev::smem_addr(cvt);
                 vbase = kbase + kTileTokens * DPAD * 2;
-            } else if constexpr (KDIRECT) {
-                vbase = dev::smem_addr(cvt);  // V is converted into the warp's f16 tile below
             }
 
             // S^T = K . q^T, two accumulator chains (even / odd k-steps)
@@ -788,16 +795,49 @@ __global__ void __launch_bounds__(kThreads)
                     break;
                 }
             }
-            if constexpr (KV8 && !KV8_APART) {
-                // V: FP8 stage -> the warp's f16 tile (the previous tile's V^T.P^T
-                // has read it); the stage is then free for tile r + S
-                __syncwarp();
-                e4m3_tile_to_f16<DPAD>(stage + TILE_BYTES, cvt, lane);
-                __syncwarp();
-                if (rn < nloc && lane == 0) issue(tmv, 1, rn, k, id_next);
-            }
             // O^T += V^T . P^T  (V rows past the range may hold anything: mask them)
             auto pv_tile = [&](uint32_t mask01, uint32_t mask89) {
+                if constexpr (VDIRECT) {
+                    // FP8 V codes straight into the A operand V^T (d x t).  The
+                    // m-tiles' rows are a permutation of d: row r of m-tile mt
+                    // is d = 128*(mt/8) + 16*(r%8) + 2*(mt%8) + r/8, so that the
+                    // rows tq, tq+8 this thread holds are two neighbouring codes
+                    // and all its rows of a 128-code box are one 16-byte chunk
+                    // of each token row.  The thread reads that chunk of its
+                    // four token rows 2qd, 2qd+1, 2qd+8, 2qd+9 (chunk tq sits at
+                    // tq ^ (t & 7) under the swizzle: every quarter-warp covers
+                    // the 32 banks once) and pairs the tokens of each code by
+                    // byte permutes: {t, t+1} of codes d, d+1 -> two f16x2.
+                    const int qd = lane & 3;
+#pragma unroll
+                    for (int bx = 0; bx < DPAD / 128; ++bx) {
+                        uint32_t R[4][4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int t = 2 * qd + (j & 1) + (j >> 1) * 8;
+                            dev::lds_v4(vbase + bx * (kTileTokens * 128) + t * 128 + ((tq ^ (t & 7)) << 4),
+                                        R[j][0], R[j][1], R[j][2], R[j][3]);
+                        }
+#pragma unroll
+                        for (int m8 = 0; m8 < 8; ++m8) {
+                            const int mt = bx * 8 + m8;
+                            const uint32_t sel = (m8 & 1) ? 0x7362u : 0x5140u;
+                            uint32_t a0, a1, a2, a3;
+                            dev::e4m3x4_to_f16x4(dev::prmt(R[0][m8 >> 1], R[1][m8 >> 1], sel), a0, a1);
+                            dev::e4m3x4_to_f16x4(dev::prmt(R[2][m8 >> 1], R[3][m8 >> 1], sel), a2, a3);
+                            a0 &= mask01;
+                            a1 &= mask01;
+                            a2 &= mask89;
+                            a3 &= mask89;
+#pragma unroll
+                            for (int nt = 0; nt < GN; ++nt) {
+                                mma_16816<true>(o[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                                if constexpr (!HL) mma_16816<true>(o[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                            }
+                        }
+                    }
+                    return;
+                }
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t a0, a1, a2, a3;
@@ -821,7 +861,7 @@ __global__ void __launch_bounds__(kThreads)
                         (tv0 + 8 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 9 < nvalid ? 0xffff0000u : 0u));
             }
             // the V half is read: refill it with tile r + S
-            if constexpr (!KV8) {
+            if constexpr (!KV8 || VDIRECT) {
                 if (rn < nloc) {
                     __syncwarp();
                     if (lane == 0) issue(tmv, 1, rn, k, id_next);
@@ -876,7 +916,9 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int g = nt * 8 + gq + (c & 1);
-                    const int d = mt * 16 + tq + (c >> 1) * 8;
+                    // the accumulator row -> d (FP8 V read directly: the permuted rows)
+                    const int d = VDIRECT ? (mt >> 3) * 128 + 16 * tq + 2 * (mt & 7) + (c >> 1)
+                                          : mt * 16 + tq + (c >> 1) * 8;
                     if (g - nt * 8 < GCOLS) wo[(warp * RT + g) * OSTRIDE + d] = o[mt][nt][c];
                 }
         __syncthreads();

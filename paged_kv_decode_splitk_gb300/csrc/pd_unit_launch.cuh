@@ -12,11 +12,13 @@ namespace pd {
 template <int DPAD, int GN, bool HL, int MODE, bool PACKED, bool KV8>
 cudaError_t launch_unit(const CUtensorMap *tmk, const CUtensorMap *tmv, const UnitParams &p_in,
                         long long units, int stages_seq, cudaStream_t stream, int layout) {
-    auto kern = unit_kernel<DPAD, GN, HL, MODE, PACKED, KV8>;
-    // Per device: the dynamic shared-memory limit raised so far, the SM count,
-    // and how many CTAs of this kernel fit on one SM at each stage count.
+    auto kern = unit_kernel<DPAD, GN, HL, MODE, PACKED, KV8, false>;
+    // Per device: the dynamic shared-memory limit raised so far (for this kernel
+    // and its 128-register twin), the SM count, and how many CTAs of this kernel
+    // fit on one SM at each stage count.
     static std::mutex mu;
     static int configured[64] = {0};
+    static int configured_cap4[64] = {0};
     static int sm_count[64] = {0};
     static int per_sm[64][kMaxStagesPerWarp + 1] = {};
     int dev = 0;
@@ -78,6 +80,25 @@ cudaError_t launch_unit(const CUtensorMap *tmk, const CUtensorMap *tmv, const Un
     // previous kernel drains, i.e. a grid of about one wave; CTAs of later
     // waves would just read the lengths and the block table twice.
     if (grid_x * 4 > static_cast<long long>(slots) * 5) p.prefetch_tiles = 0;
+    // Many waves of one-CTA units over an FP8 cache at head dim 128, groups of
+    // up to 4: the 128-register twin (4 CTAs per SM instead of 3; measured
+    // 471 -> 413 us on the 256-sequence FP8 step, while the one-wave
+    // long-context FP8 step runs 22.4 us on this kernel against 25-26 us on
+    // the twin).  Same arithmetic, same bits.
+    constexpr bool kHasCap4 = KV8 && DPAD == 128 && GN == 1 && HL && MODE == kModePaged && !PACKED;
+    bool cap4 = false;
+    if constexpr (kHasCap4) {
+        if (C == 1 && grid_x > slots) {
+            std::lock_guard<std::mutex> lock(mu);
+            if (configured_cap4[dev] < smem_bytes) {
+                e = cudaFuncSetAttribute(unit_kernel<DPAD, GN, HL, MODE, PACKED, KV8, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+                if (e != cudaSuccess) return e;
+                configured_cap4[dev] = smem_bytes;
+            }
+            cap4 = true;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_x));
     cfg.blockDim = dim3(kThreads);
@@ -107,6 +128,9 @@ cudaError_t launch_unit(const CUtensorMap *tmk, const CUtensorMap *tmv, const Un
     for (int i = 0; i < nmaps; ++i) {
         maps.k[i] = tmk[i];
         maps.v[i] = tmv[i];
+    }
+    if constexpr (kHasCap4) {
+        if (cap4) return cudaLaunchKernelEx(&cfg, unit_kernel<DPAD, GN, HL, MODE, PACKED, KV8, true>, maps, p);
     }
     return cudaLaunchKernelEx(&cfg, kern, maps, p);
 }

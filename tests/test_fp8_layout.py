@@ -14,7 +14,8 @@ the kernel's comments state them, that
 * the q reordering is a permutation;
 * each half-warp's 8-byte shared loads touch the 32 banks once (no conflict).
 
-No GPU: the GPU parity tests cover the kernel itself."""
+The same is checked for the direct V operand (below).  No GPU: the GPU
+parity tests cover the kernel itself."""
 
 import numpy as np
 import pytest
@@ -107,3 +108,86 @@ def test_the_first_mapping_had_a_two_way_conflict():
         a = tq * 128 + ch * 16 + (qd & 1) * 8
         banks += [(a // 4) % 32, (a // 4 + 1) % 32]
     assert max(np.bincount(banks, minlength=32)) == 2
+
+
+# ---- the direct V operand (V^T . P^T) -----------------------------------------------------
+# From head dim 128 up V's codes also go straight from the 128-byte-swizzled
+# tile into the A operand V^T (rows d, columns t) of mma m16n8k16.  Row r of
+# m-tile mt stands for d = 128*(mt//8) + 16*(r%8) + 2*(mt%8) + r//8; the lane
+# (tq, qd) reads, per 128-code box, 16-byte chunk tq of token rows 2qd, 2qd+1,
+# 2qd+8, 2qd+9 (at chunk tq ^ (t & 7)), and builds its four registers from
+# byte permutes of those words with selector 0x5140 (even mt) or 0x7362 (odd).
+
+
+def v_row_d(mt: int, r: int) -> int:
+    return 128 * (mt // 8) + 16 * (r % 8) + 2 * (mt % 8) + r // 8
+
+
+def prmt(a: int, b: int, sel: int) -> int:
+    """PTX prmt.b32 (default mode): byte i of the result is byte (sel >> 4i) & 7
+    of the eight bytes {b, a}."""
+    src = [(a >> (8 * i)) & 0xFF for i in range(4)] + [(b >> (8 * i)) & 0xFF for i in range(4)]
+    return sum(src[(sel >> (4 * i)) & 7] << (8 * i) for i in range(4))
+
+
+def v_direct_operands(smem: np.ndarray, D: int, lane: int):
+    """The A registers lane builds for each m-tile: {mt: (a0, a1, a2, a3)}, each
+    register a (low, high) pair of codes."""
+    tq, qd = lane >> 2, lane & 3
+    regs = {}
+    for bx in range(D // 128):
+        R = []
+        for j in range(4):
+            t = 2 * qd + (j & 1) + (j >> 1) * 8
+            base = bx * 2048 + t * 128 + ((tq ^ (t & 7)) << 4)
+            chunk = smem[base:base + 16]
+            R.append([int(chunk[4 * w]) | int(chunk[4 * w + 1]) << 8 | int(chunk[4 * w + 2]) << 16
+                      | int(chunk[4 * w + 3]) << 24 for w in range(4)])
+        for m8 in range(8):
+            sel = 0x7362 if m8 & 1 else 0x5140
+            x01 = prmt(R[0][m8 >> 1], R[1][m8 >> 1], sel)
+            x89 = prmt(R[2][m8 >> 1], R[3][m8 >> 1], sel)
+            split = lambda x: ((x & 0xFF, (x >> 8) & 0xFF), ((x >> 16) & 0xFF, (x >> 24) & 0xFF))
+            (a0, a1), (a2, a3) = split(x01), split(x89)
+            regs[bx * 8 + m8] = (a0, a1, a2, a3)
+    return regs
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_direct_v_operand_is_v_transposed_on_permuted_rows(D):
+    rng = np.random.default_rng(D + 7)
+    V = rng.integers(0, 256, size=(16, D)).astype(np.int64)
+    smem = swizzled_tile(V)
+    KS = D // 16
+    A = np.full((KS, 16, 16), -1, dtype=np.int64)   # [mt][row][token]
+    for lane in range(32):
+        tq, qd = lane >> 2, lane & 3
+        for mt, (a0, a1, a2, a3) in v_direct_operands(smem, D, lane).items():
+            # m16n8k16 A fragment: a0 (row tq, k 2qd..+1), a1 (row tq+8, k 2qd..),
+            # a2 (row tq, k 2qd+8..), a3 (row tq+8, k 2qd+8..); low half = lower k
+            for reg, row, k0 in ((a0, tq, 2 * qd), (a1, tq + 8, 2 * qd), (a2, tq, 2 * qd + 8),
+                                 (a3, tq + 8, 2 * qd + 8)):
+                A[mt, row, k0], A[mt, row, k0 + 1] = reg
+    assert (A >= 0).all(), "every operand element is written"
+    for mt in range(KS):
+        for r in range(16):
+            assert np.array_equal(A[mt, r], V[:, v_row_d(mt, r)]), (mt, r)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_direct_v_rows_are_a_permutation_of_d(D):
+    ds = sorted(v_row_d(mt, r) for mt in range(D // 16) for r in range(16))
+    assert ds == list(range(D))
+
+
+def test_direct_v_loads_cover_every_bank_once_per_quarter_warp():
+    # a 16-byte load is served a quarter-warp (8 lanes) at a time
+    for j in range(4):
+        for quarter in range(4):
+            banks = []
+            for lane in range(8 * quarter, 8 * quarter + 8):
+                tq, qd = lane >> 2, lane & 3
+                t = 2 * qd + (j & 1) + (j >> 1) * 8
+                a = t * 128 + ((tq ^ (t & 7)) << 4)
+                banks += [(a // 4 + i) % 32 for i in range(4)]
+            assert sorted(banks) == list(range(32)), (j, quarter)

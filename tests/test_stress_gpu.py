@@ -123,3 +123,35 @@ def test_three_streams_at_once_match_solo_runs(cuda_device):
     finally:
         torch.cuda.synchronize()
         t.close()
+
+
+def test_split_launches_with_their_own_workspaces_on_two_streams(cuda_device):
+    """Two split launches (partial pass + merge pass each) at once, each with its
+    own workspace, on two streams, five times: every output equals the launch
+    made alone."""
+    wa = W.custom([9000, 300, 2600], 24, 8, 128, seed=54)
+    wb = W.custom([5000, 17, 4000, 1200], 16, 4, 128, seed=55)
+    ia, ib = api.PagedInputs(wa, cuda_device), api.PagedInputs(wb, cuda_device)
+    ws_a = api.workspace(wa.num_seqs, 24, 128, 13, cuda_device)
+    ws_b = api.workspace(wb.num_seqs, 16, 128, 7, cuda_device)
+    oa = torch.empty((wa.num_seqs, 24, 128), dtype=torch.bfloat16, device=cuda_device)
+    ob = torch.empty((wb.num_seqs, 16, 128), dtype=torch.bfloat16, device=cuda_device)
+
+    def launch(stream):
+        sa, sb = stream if stream else (None, None)
+        assert api.run_paged(ia, num_splits=13, gqa_pack=0, out=oa, ws=ws_a, stream=sa) is not None
+        assert api.run_paged(ib, num_splits=7, gqa_pack=0, out=ob, ws=ws_b, stream=sb) is not None
+
+    launch(None)
+    torch.cuda.synchronize()
+    solo_a, solo_b = oa.clone(), ob.clone()
+    streams = (torch.cuda.Stream(device=cuda_device), torch.cuda.Stream(device=cuda_device))
+    for rep in range(5):
+        oa.zero_()
+        ob.zero_()
+        torch.cuda.synchronize()
+        launch(streams)
+        torch.cuda.synchronize()
+        assert pd.pd_device_status() == 0
+        assert torch.equal(oa.view(torch.int16), solo_a.view(torch.int16)), rep
+        assert torch.equal(ob.view(torch.int16), solo_b.view(torch.int16)), rep
