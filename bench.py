@@ -262,6 +262,11 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
 
     w = _workload(args.workload)
+    if args.seqs:
+        from paged_kv_decode_splitk_gb300 import workloads as W
+        if not hasattr(w, "context_lens"):
+            raise SystemExit("--seqs applies to the paged workloads only")
+        w = W.first_seqs(w, args.seqs)
     mixed = args.workload == "tiled_mixed"
     tiled = args.workload == "tiled" or mixed
     kv_bytes = w.kv_bytes
@@ -693,6 +698,9 @@ def main():
                     choices=["tiny", "gqa_packed", "gqa_packed_splitk", "gqa_packed_long", "gqa_packed_long_splitk",
                              "long_context", "large_batch", "tiled", "tiled_mixed", "gqa_packed_fp8",
                              "long_context_fp8", "large_batch_fp8"])
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="paged workloads: run only the first N sequences (a smaller case of the same "
+                         "recipe, for profiler captures); not a bench line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tiled-separate", action="store_true",

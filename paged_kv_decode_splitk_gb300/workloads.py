@@ -236,6 +236,27 @@ def gqa_packed_fp8(seed: int = SEED_VALUES) -> PagedWorkload:
     return fp8_variant(gqa_packed(seed), seed=seed)
 
 
+def first_seqs(w: PagedWorkload, n: int) -> PagedWorkload:
+    """The first n sequences of a paged workload, with a cache holding only their
+    blocks (same values; a block keeps its place relative to the others), so a
+    profiler capture of the same recipe fits in a few GB."""
+    n = max(1, min(int(n), w.num_seqs))
+    bs = w.block_size
+    need = [-(-int(L) // bs) for L in w.context_lens[:n]]
+    used = np.unique(np.concatenate([w.block_table[s, :k] for s, k in enumerate(need)] or
+                                    [np.zeros(0, np.int32)])).astype(np.int64)
+    remap = np.full(w.num_blocks, -1, dtype=np.int64)
+    remap[used] = np.arange(used.size)
+    bt = np.zeros((n, max(1, max(need) if need else 1)), dtype=np.int32)
+    for s, k in enumerate(need):
+        bt[s, :k] = remap[w.block_table[s, :k]]
+    kw = dict(w.__dict__)
+    kw.update(name=f"{w.name}_first{n}", q=w.q[:n], k_cache=w.k_cache[used] if used.size else w.k_cache[:1],
+              v_cache=w.v_cache[used] if used.size else w.v_cache[:1], block_table=bt,
+              context_lens=w.context_lens[:n].copy())
+    return PagedWorkload(**kw)
+
+
 def custom(lens, num_q_heads, num_kv_heads, head_dim, block_size=16, seed=SEED_VALUES,
            **kw) -> PagedWorkload:
     """Any shape, same recipe (used for edge cases and ragged tails)."""

@@ -84,3 +84,19 @@ def test_gqa_packed_long_pair():
     assert b.gqa_pack == 2 and P.num_splits(P.POLICY_AUTO, 0, b.sm_count, b.num_q_heads, 2, 0) == 16
     assert np.array_equal(a.k_cache, b.k_cache) and np.array_equal(a.block_table, b.block_table)
     assert np.array_equal(a.q, b.q)
+
+
+def test_first_seqs_keeps_values_and_compacts_the_cache():
+    """A sub-batch for profiler captures: the first n sequences, the same K/V rows
+    through a cache that holds only their blocks."""
+    w = W.custom([37, 300, 1000, 5, 2049], 8, 2, 64, seed=12)
+    sub = W.first_seqs(w, 3)
+    assert sub.num_seqs == 3 and sub.context_lens.tolist() == [37, 300, 1000]
+    assert np.array_equal(sub.q, w.q[:3])
+    need = [-(-int(L) // 16) for L in sub.context_lens]
+    assert sub.num_blocks == sum(need)
+    for s, k in enumerate(need):
+        for j in range(k):
+            assert np.array_equal(sub.k_cache[sub.block_table[s, j]], w.k_cache[w.block_table[s, j]])
+            assert np.array_equal(sub.v_cache[sub.block_table[s, j]], w.v_cache[w.block_table[s, j]])
+    _placement_ok(sub)
