@@ -915,11 +915,12 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
             for (int nt = 0; nt < GN; ++nt)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
+                    // row slot mt*16 + r of the accumulators (r = tq, tq + 8): d itself, or
+                    // with FP8 V read directly a permutation of d that the sum below undoes
+                    // (stored by slot, a warp's stores hit distinct banks)
                     const int g = nt * 8 + gq + (c & 1);
-                    // the accumulator row -> d (FP8 V read directly: the permuted rows)
-                    const int d = VDIRECT ? (mt >> 3) * 128 + 16 * tq + 2 * (mt & 7) + (c >> 1)
-                                          : mt * 16 + tq + (c >> 1) * 8;
-                    if (g - nt * 8 < GCOLS) wo[(warp * RT + g) * OSTRIDE + d] = o[mt][nt][c];
+                    const int slot = mt * 16 + tq + (c >> 1) * 8;
+                    if (g - nt * 8 < GCOLS) wo[(warp * RT + g) * OSTRIDE + slot] = o[mt][nt][c];
                 }
         __syncthreads();
 
@@ -940,12 +941,15 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
             cl[tid] = Lsum;
         }
         __syncthreads();
-        // the part's o: warp partials weighted and summed in warp order
+        // the part's o: warp partials weighted and summed in warp order (walked by
+        // slot; slot mt*16 + r holds d = 128*(mt/8) + 16*(r%8) + 2*(mt%8) + r/8
+        // when FP8 V was read directly, else d = slot)
         for (int e = tid; e < Gt * DPAD; e += kThreads) {
-            const int g = e / DPAD, d = e - g * DPAD;
+            const int g = e / DPAD, sl = e - g * DPAD;
+            const int d = VDIRECT ? (sl >> 7) * 128 + 16 * (sl & 7) + 2 * ((sl >> 4) & 7) + ((sl >> 3) & 1) : sl;
             float acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) acc += ww[w * RT + g] * wo[(w * RT + g) * OSTRIDE + d];
+            for (int w = 0; w < kWarps; ++w) acc += ww[w * RT + g] * wo[(w * RT + g) * OSTRIDE + sl];
             co[g * OSTRIDE + d] = acc;
         }
         if (C == 1) {

@@ -191,3 +191,29 @@ def test_direct_v_loads_cover_every_bank_once_per_quarter_warp():
                 a = t * 128 + ((tq ^ (t & 7)) << 4)
                 banks += [(a // 4 + i) % 32 for i in range(4)]
             assert sorted(banks) == list(range(32)), (j, quarter)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_combine_slot_map_undoes_the_v_row_permutation(D):
+    """The warps store their accumulators by slot mt*16 + r and the part's sum
+    writes slot sl to d = 128*(sl>>7) + 16*(sl&7) + 2*((sl>>4)&7) + ((sl>>3)&1):
+    that must be the row map of the direct V operand, slot by slot."""
+    for sl in range(D):
+        d = 128 * (sl >> 7) + 16 * (sl & 7) + 2 * ((sl >> 4) & 7) + ((sl >> 3) & 1)
+        assert d == v_row_d(sl // 16, sl % 16)
+
+
+def test_slot_order_stores_cover_distinct_banks():
+    # the warp-merge stores of one (m-tile, accumulator) for the 16 lanes of the
+    # first 4 groups (HL: columns 0..3): row (warp*8 + g) of stride DPAD + 4
+    # floats, column slot = mt*16 + tq + 8*(c>>1) -- distinct banks
+    OST = 128 + 4
+    for mt in range(8):
+        for c in range(4):
+            banks = []
+            for lane in range(32):
+                tq, qd = lane >> 2, lane & 3
+                g = 2 * qd + (c & 1)
+                if g < 4:
+                    banks.append((g * OST + mt * 16 + tq + 8 * (c >> 1)) % 32)
+            assert len(set(banks)) == len(banks), (mt, c)
