@@ -419,6 +419,8 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     achieved = kv_bytes / (unit_ms / 1e3) / 1e9
     kernel_tag = "unit_packed" if w.__dict__.get("gqa_pack") else ("unit_tiled" if tiled else "unit_splitk")
+    if tiled and not mixed and args.tiled_separate:
+        kernel_tag = "unit_tiledstep"  # one launch per step_tile call: not the fused run's kernel
     traffic = _traffic_from_profiles(kernel_tag, args.workload)
 
     # ---- end to end: host buffers through the public API ----
