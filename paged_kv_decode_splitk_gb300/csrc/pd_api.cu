@@ -259,16 +259,30 @@ int default_lpt(int num_seqs) {
 // to max_parts parts of about kPartTiles 16-token tiles, by its own length; the
 // parts fold in order.  Build constants: they fix the summation order.
 constexpr int kPartTiles = 32;
-// Bytes of K/V at the start of its part that a paged-mode CTA prefetches into
-// L2 before it waits for the previous kernel (a scheduling hint: it changes no
-// result); a 16-token K+V tile holds 64 * dpad bytes.
+// K/V tiles at the start of its part that a paged-mode CTA of a one-wave launch
+// prefetches into L2 before it waits for the previous kernel (a scheduling
+// hint: it changes no result): as many tiles as 128 KB of a BF16 cache holds
+// (a 16-token K+V tile is 64 * dpad bytes), for an FP8 cache the same number
+// of tiles.  Measured on one box, A/B: 64 / 192 / 256 / 384 / 512 KB of BF16
+// tiles were slower on the long-context, packed and packed-with-splits steps
+// (up to 15%); over an FP8 cache, the same tile count (64 KB) beat 128 KB by 4%
+// on the packed step and 1% on the long-context one.
 constexpr int kPrefetchBytes = 128 * 1024;
-// Cluster sizes: 8 at D = 256; at D <= 128 five for BF16 (a 158-tile split in
-// 5 CTAs of 4 warps still fits one wave at 4 CTAs per SM: measured 27.3 ->
-// 26.9 us on the long-context workload), four for FP8 (3 CTAs per SM there).
-int max_parts_for(int dpad, bool tiled, bool kv8 = false) {
+// Cluster sizes (every unit of a cluster launch gets max_parts ranks, and the
+// ranks beyond its parts only hold a slot until they see its length):
+// * D <= 128: five for BF16 (a 158-tile split in 5 CTAs of 4 warps still fits
+//   one wave at 4 CTAs per SM: measured 27.3 -> 26.9 us on the long-context
+//   workload; 3 and 4 were slower), four for FP8 (3 CTAs per SM there; 3 and
+//   5 slower).
+// * D = 256: seven, so that 64 packed units x 7 CTAs fit the 456 slots of one
+//   wave (measured on the packed step against 8: BF16 31.9 -> 30.9 us, FP8
+//   27.6 -> 26.2 us; 6 and 4 slower); four for the packed pass with splits
+//   (the splits already supply the parallelism: 33.0 -> 30.1 us on two
+//   32768-token sequences at 16 splits).  A launch with one split keeps the
+//   packed pass's seven, so both packed modes give the same bits there.
+int max_parts_for(int dpad, bool tiled, bool kv8 = false, bool packed_splits = false) {
     if (tiled) return 2;
-    if (dpad >= 256) return 8;
+    if (dpad >= 256) return packed_splits ? 4 : 7;
     return kv8 ? 4 : 5;
 }
 
@@ -559,7 +573,8 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     const int qtiles = (G + rows - 1) / rows;
     const int stages = default_stages(dpad, kv8);
     const long long units = static_cast<long long>(num_seqs) * num_kv_heads * qtiles * num_splits;
-    if (units * max_parts_for(dpad, false, kv8) > 0x7fffffffLL)
+    const bool packed_splits = gqa_pack == PD_GQA_PACK_SPLITK && num_splits > 1;
+    if (units * max_parts_for(dpad, false, kv8, packed_splits) > 0x7fffffffLL)
         return fail(PD_ERR_INVALID, "launch too large (%lld units)", units);
 
     int err = PD_OK;
@@ -605,11 +620,11 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     p.block_size = block_size;
     p.qtiles = qtiles;
     p.cluster = 1;
-    p.max_parts = max_parts_for(dpad, false, kv8);
+    p.max_parts = max_parts_for(dpad, false, kv8, packed_splits);
     p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = default_lpt(num_seqs);
-    p.prefetch_tiles = kPrefetchBytes / (2 * pd::kTileTokens * dpad * elem);
+    p.prefetch_tiles = kPrefetchBytes / (2 * pd::kTileTokens * dpad * 2);
     p.tok_dim = tok_dim;
     // An FP8 cache's K scale multiplies every score: fold it into the softmax scale.
     p.scale_log2 = static_cast<float>(static_cast<double>(inv_sqrt_d) * (kv8 ? static_cast<double>(k_scale) : 1.0) *
