@@ -229,10 +229,11 @@ int encode_kv_map_uncached(CUtensorMap *map, int *tok_dim, const void *base, int
 
 // ---- launch choices ----------------------------------------------------------------
 // Stages per warp of the unit pipeline.  A single-wave launch keeps about
-// 32-64 KB of K/V in flight per CTA so that three or four CTAs share an SM; a
-// launch of several waves of one-CTA units (each unit short, its start-up
-// latency exposed) doubles the ring at head dims up to 128, measured ~3%
-// faster on the large-batch workload at D = 128.
+// 32-64 KB of K/V in flight per CTA so that three or four CTAs share an SM.  A
+// launch of several waves of one-CTA units keeps one stage at D = 128 too, so
+// that four CTAs share an SM (measured A/B on the large-batch workload: 494 us
+// at one stage against 512 us at two and 615 us at three); at D = 64 it
+// doubles the ring, and over an FP8 cache two stages and one run alike.
 int g_debug_stages = 0;
 int g_debug_cluster = 0;
 int g_debug_lpt = -1;
@@ -246,7 +247,7 @@ int default_stages(int dpad, bool kv8 = false) {
 int default_stages_seq(int dpad, bool kv8 = false) {
     if (g_debug_stages > 0) return g_debug_stages;
     if (kv8) return 2;  // measured: 4 stages cost a CTA per SM at D = 128
-    return dpad <= 128 ? 2 : 1;
+    return dpad <= 64 ? 2 : 1;
 }
 
 // Longest-first service order for small batches (a scheduling choice only).
