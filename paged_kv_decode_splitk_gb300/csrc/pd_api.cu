@@ -257,9 +257,9 @@ int default_lpt(int num_seqs) {
 }
 
 // A unit's range (one split of a sequence, or one tile of it) is cut into up
-// to max_parts parts of about kPartTiles 16-token tiles, by its own length; the
-// parts fold in order.  Build constants: they fix the summation order.
-constexpr int kPartTiles = 32;
+// to max_parts parts of about pd::kPartTiles 16-token tiles, by its own
+// length; the parts fold in order.  Build constants: they fix the summation
+// order.
 // K/V tiles at the start of its part that a paged-mode CTA of a one-wave launch
 // prefetches into L2 before it waits for the previous kernel (a scheduling
 // hint: it changes no result): as many tiles as 128 KB of a BF16 cache holds
@@ -621,8 +621,9 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     p.block_size = block_size;
     p.qtiles = qtiles;
     p.cluster = 1;
+    p.fd_bs = pd::make_fastdiv(p.block_size);
+    p.fd_split = pd::make_fastdiv(num_splits);
     p.max_parts = max_parts_for(dpad, false, kv8, packed_splits);
-    p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = default_lpt(num_seqs);
     p.prefetch_tiles = kPrefetchBytes / (2 * pd::kTileTokens * dpad * 2);
@@ -886,8 +887,9 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     p.block_size = d.block_size;
     p.qtiles = qtiles;
     p.cluster = 1;
+    p.fd_bs = pd::make_fastdiv(p.block_size);
+    p.fd_split = pd::make_fastdiv(1);
     p.max_parts = max_parts_for(dpad, true);
-    p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = 0;
     // No early prefetch in the tiled step: measured no gain (the begin pass or
@@ -980,8 +982,9 @@ int tiled_run_fused(pd_tiled *t, const void *q, const pd_tiled_source *sources, 
     p.block_size = d.block_size;
     p.qtiles = qtiles;
     p.cluster = 1;
+    p.fd_bs = pd::make_fastdiv(p.block_size);
+    p.fd_split = pd::make_fastdiv(1);
     p.max_parts = max_parts_for(dpad, true);
-    p.part_tiles = kPartTiles;
     p.stages = stages;
     p.lpt = 0;
     p.prefetch_tiles = 0;

@@ -35,6 +35,55 @@ __host__ __device__ inline int splits_used(int context_len, int chunk) {
     return context_len > 0 ? (context_len + chunk - 1) / chunk : 0;
 }
 
+// Tiles (16 tokens each) a part of a unit's range aims for: the range is cut
+// into ceil(tiles / kPartTiles) parts, at most max_parts.
+constexpr int kPartTiles = 32;
+
+// Division by a divisor fixed for a launch, as a multiply-high, an add and a
+// shift (T. Granlund and P. L. Montgomery, "Division by invariant integers
+// using multiplication", PLDI 1994, section 4): for a divisor d >= 1 let
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1, which is below 2^32
+// because d > 2^(l-1).  Then floor(n / d) = (mulhi(n, m) + n) >> l for every
+// 0 <= n < 2^32, and for n < 2^31 the sum cannot overflow 32 bits.  The
+// kernels use it for the split geometry, whose quotients must equal the
+// plain integer division's.
+struct FastDiv {
+    uint32_t d;  // the divisor
+    uint32_t m;  // multiplier
+    uint32_t l;  // shift
+};
+
+inline FastDiv make_fastdiv(int d) {
+    FastDiv f;
+    f.d = static_cast<uint32_t>(d < 1 ? 1 : d);
+    f.l = 0;
+    while ((uint64_t{1} << f.l) < f.d) ++f.l;
+    f.m = static_cast<uint32_t>((((uint64_t{1} << f.l) - f.d) << 32) / f.d + 1);
+    return f;
+}
+
+// floor(n / f.d) for 0 <= n < 2^31.
+__host__ __device__ inline int fast_div(int n, const FastDiv &f) {
+    const uint32_t u = static_cast<uint32_t>(n);
+#ifdef __CUDA_ARCH__
+    const uint32_t t = __umulhi(u, f.m);
+#else
+    const uint32_t t = static_cast<uint32_t>((static_cast<uint64_t>(u) * f.m) >> 32);
+#endif
+    return static_cast<int>((t + u) >> f.l);
+}
+
+// split_chunk_tokens with the split count and the block size as FastDiv
+// (same value for every argument the kernels pass: 0 <= context_len and
+// context_len + num_splits, chunk + block_size below 2^31).
+__host__ __device__ inline int split_chunk_tokens_fd(int context_len, const FastDiv &num_splits,
+                                                     const FastDiv &block_size, int min_kv_per_split) {
+    const int n = static_cast<int>(num_splits.d), bs = static_cast<int>(block_size.d);
+    int per = context_len > 0 ? fast_div(context_len + n - 1, num_splits) : 0;
+    int c = per > min_kv_per_split ? per : min_kv_per_split;
+    return fast_div(c + bs - 1, block_size) * bs;
+}
+
 enum UnitMode : int {
     kModePaged = 0,     // pd_decode_attn: block_table gather, split ranges, out / workspace
     kModeTiled = 1,     // pd_tiled_step: tile list, fold into the running state
@@ -83,9 +132,10 @@ struct UnitParams {
     // shape
     int num_seqs, num_q_heads, num_kv_heads, group, head_dim, block_size;
     int qtiles;       // CTAs per (s, kvh): ceil(group / rows per CTA)
+    FastDiv fd_split;    // num_splits (paged mode; 1 otherwise), for the split geometry
+    FastDiv fd_bs;       // block_size
     int cluster;      // CTAs per unit: 1 (parts in sequence) or max_parts (one part per CTA)
     int max_parts;    // parts a unit's range is cut into at most
-    int part_tiles;   // tiles per part the cut aims for
     int stages;       // pipeline stages per warp
     int lpt;          // paged mode: serve sequences longest first (needs num_seqs <= kLptMaxSeqs)
     int prefetch_tiles;  // first tiles of the CTA's part prefetched into L2 before the wait (0: none)

@@ -13,7 +13,7 @@
 //
 // GB300 mapping:
 //   * The unit's range of 16-token tiles is cut into V length-defined parts
-//     (V = clamp(ceil(tiles / part_tiles), 1, max_parts)).  A CTA of kWarps
+//     (V = clamp(ceil(tiles / kPartTiles), 1, max_parts)).  A CTA of kWarps
 //     warps takes a part; warp w folds its tiles w, w+kWarps, ... with its own
 //     online-softmax state and the warps merge in warp order.  The parts fold
 //     left to right with pinned rounding, either in one CTA walking them in
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
             ss = p.lpt ? longest_first(true) : s;
             int L = __ldcg(p.context_lens + ss);
             L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
-            const int chunk = split_chunk_tokens(L, p.num_splits, bs, p.min_kv_per_split);
+            const int chunk = split_chunk_tokens_fd(L, p.fd_split, p.fd_bs, p.min_kv_per_split);
             const long long a = static_cast<long long>(split) * chunk;
             t0 = static_cast<int>(a < L ? a : L);
             t1 = static_cast<int>(a + chunk < L ? a + chunk : L);
@@ -305,16 +305,17 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         if (t0 < t1) {
             const int tile0 = t0 / kTileTokens;
             const int ntiles = (t1 + kTileTokens - 1) / kTileTokens - tile0;
-            const int V = max(1, min(p.max_parts, (ntiles + p.part_tiles - 1) / p.part_tiles));
+            const int V = max(1, min(p.max_parts, (ntiles + kPartTiles - 1) / kPartTiles));
             const int j = C == 1 ? 0 : part;
             if (j < V) {
                 const int my0 = tile0 + (j * ntiles) / V;
                 const int n = min(tile0 + ((j + 1) * ntiles) / V - my0, p.prefetch_tiles);
                 for (int t = tid; t < n; t += kThreads) {
                     const int gt = my0 + t;
-                    const int id = __ldcg(ids + gt / tiles_per_block);
+                    const int blk = tiles_per_block > 1 ? gt / tiles_per_block : gt;
+                    const int id = __ldcg(ids + blk);
                     if (id >= 0 && id < p.num_blocks) {
-                        const int sub = (gt % tiles_per_block) * kTileTokens;
+                        const int sub = (gt - blk * tiles_per_block) * kTileTokens;
                         const int c1 = tok_dim == 1 ? sub : kvh;
                         const int c2 = tok_dim == 1 ? kvh : sub;
                         if constexpr (KDIRECT) {
@@ -373,11 +374,11 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                 dev::flag_status(p.status, kDevBadContextLen);
             L = L < 0 ? 0 : Lmax;
         }
-        const int chunk = split_chunk_tokens(L, p.num_splits, bs, p.min_kv_per_split);
+        const int chunk = split_chunk_tokens_fd(L, p.fd_split, p.fd_bs, p.min_kv_per_split);
         const long long a = static_cast<long long>(split) * chunk;
         tok0 = static_cast<int>(a < L ? a : L);
         tok1 = static_cast<int>(a + chunk < L ? a + chunk : L);
-        direct = splits_used(L, chunk) <= 1;
+        direct = L <= chunk;  // at most one non-empty split
         ids_base = p.block_table + static_cast<long long>(s) * p.max_blocks_per_seq;
         if (tok0 >= tok1) {
             // Empty split.  Split 0 of an empty sequence owns the zero output.
@@ -406,13 +407,13 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         ids_base = (RUN ? p.src_blocks[split] : p.tile_blocks) + static_cast<long long>(s) * p.tile_capacity;
     }
 
-    // 16-token tiles of the range, cut into V parts of about p.part_tiles tiles
+    // 16-token tiles of the range, cut into V parts of about kPartTiles tiles
     // (at most p.max_parts).  V depends only on the range's own length; the
     // launch decides only where the parts run: all in this CTA one after
     // another (cluster == 1), or one per CTA of a cluster (cluster == max_parts).
     const int tile0 = tok0 / kTileTokens;
     const int ntiles = (tok1 + kTileTokens - 1) / kTileTokens - tile0;
-    const int V = max(1, min(p.max_parts, (ntiles + p.part_tiles - 1) / p.part_tiles));
+    const int V = max(1, min(p.max_parts, (ntiles + kPartTiles - 1) / kPartTiles));
     // A rank of a cluster beyond the unit's parts has nothing to do: no peer
     // reads or signals it, so it leaves now and frees its slot.
     if (C > 1 && part >= V) return;
@@ -526,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         auto load_id = [&](int r) -> int {
             if (r >= nloc) return -1;
             const int gt = my0 + warp + kWarps * r;
-            int id = __ldg(ids_base + gt / tiles_per_block);
+            int id = __ldg(ids_base + (tiles_per_block > 1 ? gt / tiles_per_block : gt));
             // TMA reads zeros outside the tensor map's block extent (num_blocks).
             if (id < 0 || id >= p.num_blocks) dev::flag_status(p.status, kDevBadBlockId);
             return id;
@@ -534,7 +535,8 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         // TMA of the K (half 0) or V (half 1) tile of local tile r into stage k.
         auto issue = [&](const CUtensorMap *map, int half, int r, int k, int id) {
             const int gt = my0 + warp + kWarps * r;
-            const int sub = (gt % tiles_per_block) * kTileTokens;
+            int sub = 0;  // first token of the tile within its cache block
+            if (tiles_per_block > 1) sub = (gt % tiles_per_block) * kTileTokens;
             const uint32_t bar = dev::smem_addr(&bars[(warp * S + k) * 2 + half]);
             const uint32_t dst = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES + half * TILE_BYTES);
             const int c1 = tok_dim == 1 ? sub : kvh;
@@ -564,12 +566,17 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
             const int b = __shfl_sync(0xffffffffu, id_nxt, r & 31);
             return (r >> 5) == win ? a : b;
         };
+        // Ring position of local tile 0: stage k with phase parity par; the
+        // tiles take the stages in turn, the parity flipping at each wrap.
+        int k = rr % S;
+        uint32_t par = (rr / S) & 1;
         const int npro = nloc < S ? nloc : S;
         for (int r = 0; r < npro; ++r) {
             const int id = __shfl_sync(0xffffffffu, id_cur, r);
+            const int kr = k + r < S ? k + r : k + r - S;
             if (lane == 0) {
-                issue(tmk, 0, r, (rr + r) % S, id);
-                issue(tmv, 1, r, (rr + r) % S, id);
+                issue(tmk, 0, r, kr, id);
+                issue(tmv, 1, r, kr, id);
             }
         }
 
@@ -597,8 +604,6 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         int fail_r = -1;
 
         for (int r = 0; r < nloc; ++r) {
-            const int k = (rr + r) % S;
-            const uint32_t par = ((rr + r) / S) & 1;
             const int rn = r + S;
             int id_next = -1;
             if (rn < nloc) {
@@ -866,6 +871,10 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                     __syncwarp();
                     if (lane == 0) issue(tmv, 1, rn, k, id_next);
                 }
+            }
+            if (++k == S) {
+                k = 0;
+                par ^= 1u;
             }
         }
         if (fail_r >= 0) {
