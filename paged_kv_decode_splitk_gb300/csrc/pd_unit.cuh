@@ -417,6 +417,9 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     // A rank of a cluster beyond the unit's parts has nothing to do: no peer
     // reads or signals it, so it leaves now and frees its slot.
     if (C > 1 && part >= V) return;
+    // A paged unit of one part: its result is that part's, in either layout
+    // (no fold into a running result, no hand-off between ranks).
+    const bool solo = MODE == kModePaged && V == 1;
 
     // ---- q to shared memory (the barriers were initialised at the start) ----------
     // Over an FP8 cache the products run in f16: q is staged as f16 scaled by a
@@ -933,6 +936,62 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                 }
         __syncthreads();
 
+        if constexpr (MODE == kModePaged && !PACKED) {
+            if (solo) {
+                // A unit of one part: each output pair straight from the warp
+                // partials, with the operations, in the order, of the general
+                // path below (part max, warp weights, sums in warp order; then
+                // the epilogue's scale and division), and no fold or hand-off.
+                // (Not compiled into the packed pass, whose units are rarely
+                // that short: measured slower there.)
+                dev::griddep_launch_dependents();
+                const int halfD = D / 2;
+                for (int e = tid; e < Gt * halfD; e += kThreads) {
+                    const int g = e / halfD;
+                    const int d = (e - g * halfD) * 2;
+                    // accumulator slots of d and d + 1 (the inverse of the FP8
+                    // direct-V permutation of d, where d + 1 sits 8 slots on)
+                    int sl0 = d, sl1 = d + 1;
+                    if constexpr (VDIRECT) {
+                        const int r = d & 127;
+                        sl0 = (d - r) + (r >> 4) + 16 * ((r >> 1) & 7);
+                        sl1 = sl0 + 8;
+                    }
+                    float M = kNegInf;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * RT + g]);
+                    float Lsum = 0.f, acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) {
+                        const float mw = wm[w * RT + g];
+                        const float wt = mw == kNegInf ? 0.f : dev::exp2_approx(mw - M);
+                        Lsum += wt * wl[w * RT + g];
+                        acc0 += wt * wo[(w * RT + g) * OSTRIDE + sl0];
+                        acc1 += wt * wo[(w * RT + g) * OSTRIDE + sl1];
+                    }
+                    const long long row = static_cast<long long>(s) * Hq + h0 + g;
+                    if constexpr (KV8) {  // V = code value * v_scale
+                        acc0 *= p.v_scale;
+                        acc1 *= p.v_scale;
+                    }
+                    if (direct) {
+                        const bool pos = Lsum > 0.f;
+                        const __nv_bfloat162 v = __floats2bfloat162_rn(pos ? __fdiv_rn(acc0, Lsum) : 0.f,
+                                                                       pos ? __fdiv_rn(acc1, Lsum) : 0.f);
+                        *reinterpret_cast<__nv_bfloat162 *>(p.out + row * D + d) = v;
+                    } else {
+                        const long long slot_row = row * p.num_splits + split;
+                        *reinterpret_cast<float2 *>(p.ws_o + slot_row * D + d) = make_float2(acc0, acc1);
+                        if (d == 0) {
+                            p.ws_ml[slot_row * 2 + 0] = M;
+                            p.ws_ml[slot_row * 2 + 1] = Lsum;
+                        }
+                    }
+                }
+                return;
+            }
+        }
+
         // part statistics of each valid row: max, warp weights, sum
         if (tid < Gt) {
             float M = kNegInf;
@@ -961,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
             for (int w = 0; w < kWarps; ++w) acc += ww[w * RT + g] * wo[(w * RT + g) * OSTRIDE + sl];
             co[g * OSTRIDE + d] = acc;
         }
-        if (C == 1) {
+        if (C == 1 && !solo) {
             // fold the part into the running result, in part order
             __syncthreads();
             if (tid < Gt) {
@@ -1000,13 +1059,14 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     // hardware cluster barrier; otherwise the idle ranks have left and the
     // active ones hand off through the ready / done mbarriers.
     cg::cluster_group cluster = cg::this_cluster();
-    const int RK = C > 1 ? V : 1;                  // ranks rows are dealt to
-    const int nown = C > 1 ? min(V, Gt) : 1;       // ranks that own a row
-    const bool full = C > 1 && V == C;
+    const bool multi = C > 1 && !solo;             // parts on several ranks
+    const int RK = multi ? V : 1;                  // ranks rows are dealt to
+    const int nown = multi ? min(V, Gt) : 1;       // ranks that own a row
+    const bool full = multi && V == C;
     if (full) {
         dev::cluster_wait();  // (the arrive at the start)
         cluster.sync();       // every part is published
-    } else if (C > 1) {
+    } else if (multi) {
         dev::cluster_wait();  // the peers' barriers are initialised
         __syncthreads();      // this part's co, cm and cl are complete
         if (tid == 0) {
@@ -1022,12 +1082,15 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                 dev::flag_status(p.status, kDevWaitTimeout);
         }
     } else {
-        // the folded o goes to shared memory for the epilogue (the ring is free)
+        // the folded o goes to shared memory for the epilogue (the ring is
+        // free); a single part's is there already
+        if (!solo) {
 #pragma unroll
-        for (int i = 0; i < RACC; ++i) {
-            const int e = tid + i * kThreads;
-            const int g = e / DPAD, d = e - g * DPAD;
-            if (g < Gt) co[g * OSTRIDE + d] = racc[i];
+            for (int i = 0; i < RACC; ++i) {
+                const int e = tid + i * kThreads;
+                const int g = e / DPAD, d = e - g * DPAD;
+                if (g < Gt) co[g * OSTRIDE + d] = racc[i];
+            }
         }
         __syncthreads();
     }
@@ -1036,7 +1099,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     if (tid < nmine) {
         const int g = part + tid * RK;
         float M = kNegInf, Lsum = 0.f;
-        if (C > 1) {
+        if (multi) {
             for (int jj = 0; jj < V; ++jj) {
                 const float mj = cluster.map_shared_rank(cm, jj)[g];
                 const float lj = cluster.map_shared_rank(cl, jj)[g];
@@ -1047,9 +1110,12 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                 fr[tid * 2 * kMaxParts + 2 * jj + 0] = fa;
                 fr[tid * 2 * kMaxParts + 2 * jj + 1] = fb;
             }
-        } else {
+        } else if (!solo) {
             M = rM[g];
             Lsum = rL[g];
+        } else {
+            M = cm[g];
+            Lsum = cl[g];
         }
         const long long row = static_cast<long long>(s) * Hq + h0 + g;
         float fa = 0.f, fb = 0.f;
@@ -1084,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         const int d = (e - i * halfD) * 2;
         const int g = part + i * RK;
         float acc0 = 0.f, acc1 = 0.f;
-        if (C > 1) {
+        if (multi) {
             float v0[kMaxParts], v1[kMaxParts];
 #pragma unroll
             for (int jj = 0; jj < kMaxParts; ++jj) {
@@ -1135,7 +1201,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     }
     if (full) {
         cluster.sync();  // peers keep their shared memory until every rank has read it
-    } else if (C > 1) {
+    } else if (multi) {
         // Tell every active rank that this owner has read it (relaxed: the
         // reads have returned, and the output stores need not drain first);
         // keep this CTA's shared memory alive until its own readers are done.
