@@ -658,6 +658,9 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
         mp.block_size = block_size;
         mp.min_kv_per_split = PD_MIN_KV_PER_SPLIT;
         mp.max_tokens = max_blocks_per_seq * block_size;
+        mp.fd_hq = pd::make_fastdiv(num_q_heads);
+        mp.fd_split = pd::make_fastdiv(num_splits);
+        mp.fd_bs = pd::make_fastdiv(block_size);
         e = pd::launch_merge(mp, st, true);
         if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
     }

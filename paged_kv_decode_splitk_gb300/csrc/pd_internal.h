@@ -152,6 +152,7 @@ struct MergeParams {
     __nv_bfloat16 *out;
     int num_seqs, num_q_heads, head_dim, num_splits, block_size, min_kv_per_split;
     int max_tokens;  // max_blocks_per_seq * block_size (context lengths are clamped to it)
+    FastDiv fd_hq, fd_split, fd_bs;  // num_q_heads, num_splits, block_size
 };
 
 // Record an error message for pd_last_error() and return `code`.

@@ -5,6 +5,7 @@
 
 #include "pd_device.cuh"
 #include "pd_internal.h"
+#include "pd.h"
 
 namespace pd {
 
@@ -13,6 +14,7 @@ namespace {
 constexpr int kMergeWarps = 8;
 constexpr int kMergeCols = 128;   // columns of a row one warp merges (4 per lane)
 constexpr int kMergeBatch = 16;   // splits whose partials are loaded together
+static_assert(PD_MAX_HEAD_DIM <= 2 * kMergeCols, "a row is at most two warps' columns");
 
 // Merge pass (Module attn_splitk page: the split-K workspace of [o, m, l]
 // slots and the non-associative merge).  One warp per (sequence, q head, 128
@@ -22,32 +24,36 @@ constexpr int kMergeBatch = 16;   // splits whose partials are loaded together
 // splits and the context length are loaded in one go, before the length says
 // which splits are non-empty (every slot of the workspace is in bounds; slots
 // past the non-empty splits are read and ignored), so the pass costs one
-// round trip to memory.  Sequences with at most one non-empty split were
-// written by the partial pass directly and are left alone here.
+// round trip to memory; the row's sequence is found before the wait on the
+// partial pass, and the split geometry divides by multiply-highs (FastDiv).
+// Split i is non-empty when i * chunk < L.  Sequences with at most one
+// non-empty split were written by the partial pass directly and are left
+// alone here.
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_constant__ MergeParams p) {
     const float kNegInf = -__int_as_float(0x7f800000);
     dev::griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int D = p.head_dim;
     const int N = p.num_splits;
-    const int chunks = (D + kMergeCols - 1) / kMergeCols;
+    const int chunks = D > kMergeCols ? 2 : 1;  // head_dim <= PD_MAX_HEAD_DIM = 2 * kMergeCols
     const long long item = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
     if (item >= static_cast<long long>(p.num_seqs) * p.num_q_heads * chunks) return;
-    const long long row = item / chunks;
+    const long long row = item >> (chunks - 1);
     const int d0 = static_cast<int>(item - row * chunks) * kMergeCols + lane * 4;
     const bool cols = d0 < D;  // D is a multiple of 8: the lane's 4 columns are all in range
+    const int s = row < 0x7fffffffLL ? fast_div(static_cast<int>(row), p.fd_hq)
+                                     : static_cast<int>(row / p.num_q_heads);
+    const float *ml = p.ws_ml + row * N * 2;
+    const float *ob = p.ws_o + row * N * D + d0;
     // Wait before any global read: the partial pass may have started before the
     // kernel ahead of it (which may write context_lens) finished, and waiting
     // for the partial pass's completion covers that kernel too.
     dev::griddep_wait();
-    const int s = static_cast<int>(row / p.num_q_heads);
     int L = p.context_lens[s];
-    const float *ml = p.ws_ml + row * N * 2;
-    const float *ob = p.ws_o + row * N * D + d0;
 
     float M = kNegInf, Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int nsu = -1;
+    long long chunk = -1;
     for (int i0 = 0; i0 < N; i0 += kMergeBatch) {
         float4 oi[kMergeBatch];
 #pragma unroll
@@ -57,15 +63,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
         // lane j holds (m, l) of split i0 + j
         float2 mlj = make_float2(kNegInf, 0.f);
         if (lane < kMergeBatch && i0 + lane < N) mlj = *reinterpret_cast<const float2 *>(ml + 2 * (i0 + lane));
-        if (nsu < 0) {
+        if (chunk < 0) {
             L = L < 0 ? 0 : (L > p.max_tokens ? p.max_tokens : L);
-            nsu = splits_used(L, split_chunk_tokens(L, N, p.block_size, p.min_kv_per_split));
+            chunk = split_chunk_tokens_fd(L, p.fd_split, p.fd_bs, p.min_kv_per_split);
+            if (L <= chunk) return;  // at most one non-empty split: written directly
         }
 #pragma unroll
         for (int j = 0; j < kMergeBatch; ++j) {
             const float mi = __shfl_sync(0xffffffffu, mlj.x, j);
             const float li = __shfl_sync(0xffffffffu, mlj.y, j);
-            if (i0 + j < nsu && mi != kNegInf) {
+            if ((i0 + j) * chunk < L && mi != kNegInf) {
                 const float Mn = fmaxf(M, mi);
                 const float a = M == kNegInf ? 0.f : dev::exp2_approx(M - Mn);
                 const float b = dev::exp2_approx(mi - Mn);
@@ -77,9 +84,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const __grid_co
                 M = Mn;
             }
         }
-        if (i0 + kMergeBatch >= nsu) break;  // the rest are empty splits
+        if ((i0 + kMergeBatch) * chunk >= L) break;  // the rest are empty splits
     }
-    if (nsu <= 1 || !cols) return;
+    if (!cols) return;
     const bool pos = Lsum > 0.f;
     __nv_bfloat162 lo = __floats2bfloat162_rn(pos ? __fdiv_rn(acc.x, Lsum) : 0.f,
                                               pos ? __fdiv_rn(acc.y, Lsum) : 0.f);
@@ -103,15 +110,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32) tiled_run_merge_kernel(const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int D = p.head_dim;
     const int T = p.num_sources;
-    const int chunks = (D + kMergeCols - 1) / kMergeCols;
+    const int chunks = D > kMergeCols ? 2 : 1;  // head_dim <= PD_MAX_HEAD_DIM = 2 * kMergeCols
     const long long item = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
     if (item >= static_cast<long long>(p.num_seqs) * p.num_q_heads * chunks) return;
-    const long long row = item / chunks;
+    const long long row = item >> (chunks - 1);
     const int chunk = static_cast<int>(item - row * chunks);
     const int d0 = chunk * kMergeCols + lane * 4;
     const bool cols = d0 < D;  // D is a multiple of 8: the lane's 4 columns are all in range
+    const int s = static_cast<int>(row / p.num_q_heads);  // (launch geometry: before the wait)
     dev::griddep_wait();  // the unit pass's partials are complete and visible
-    const int s = static_cast<int>(row / p.num_q_heads);
     int cnt[kMaxRunSources];
     float2 mli[kMaxRunSources];
     float4 oi[kMaxRunSources];
