@@ -179,6 +179,10 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     // swizzled) FP8 tiles straight into the mma operands.
     constexpr bool KDIRECT = KV8 && DPAD >= 128;
     constexpr bool VDIRECT = KDIRECT;
+    // K and V of a tile on one barrier, issued together (FP8 at head dim 128;
+    // at 256, where a tile's math takes twice as long, the packed pass
+    // measured slower with it)
+    constexpr bool KV1BAR = KV8 && DPAD == 128;
     constexpr int TILE_BYTES = kTileTokens * DPAD * (KV8 ? 1 : 2);  // one landed K or V tile
     constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static_assert(!KV8 || MODE == kModePaged, "FP8 caches are a paged-mode source");
@@ -558,6 +562,25 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                     dev::tma_load_4d(dst + b * (kTileTokens * 128), map, bar, b * kBoxCols, c1, c2, id, policy);
             }
         };
+        // KV1BAR: K and V of a tile land on one barrier (half 0), issued
+        // together after the tile's P.V, which saves a wait and an issue per
+        // tile; the two stages per warp keep the next tile in flight meanwhile.
+        auto issue_kv = [&](int r, int k, int id) {
+            const int gt = my0 + warp + kWarps * r;
+            int sub = 0;
+            if (tiles_per_block > 1) sub = (gt % tiles_per_block) * kTileTokens;
+            const uint32_t bar = dev::smem_addr(&bars[(warp * S + k) * 2]);
+            const uint32_t dst = dev::smem_addr(ring + (warp * S + k) * STAGE_BYTES);
+            const int c1 = tok_dim == 1 ? sub : kvh;
+            const int c2 = tok_dim == 1 ? kvh : sub;
+            dev::mbar_arrive_expect_tx(bar, STAGE_BYTES);
+#pragma unroll
+            for (int b = 0; b < DPAD / 128; ++b)
+                dev::tma_load_4d(dst + b * (kTileTokens * 128), tmk, bar, b * 128, c1, c2, id, policy);
+#pragma unroll
+            for (int b = 0; b < DPAD / 128; ++b)
+                dev::tma_load_4d(dst + TILE_BYTES + b * (kTileTokens * 128), tmv, bar, b * 128, c1, c2, id, policy);
+        };
 
         // Block ids of local tiles [32*win, 32*win + 64): lane l of id_cur holds
         // tile 32*win + l, lane l of id_nxt tile 32*win + 32 + l.
@@ -578,8 +601,12 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
             const int id = __shfl_sync(0xffffffffu, id_cur, r);
             const int kr = k + r < S ? k + r : k + r - S;
             if (lane == 0) {
-                issue(tmk, 0, r, kr, id);
-                issue(tmv, 1, r, kr, id);
+                if constexpr (KV1BAR) {
+                    issue_kv(r, kr, id);
+                } else {
+                    issue(tmk, 0, r, kr, id);
+                    issue(tmv, 1, r, kr, id);
+                }
             }
         }
 
@@ -704,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
             // The K half is read (every lane's ldmatrix result has been consumed by
             // an mma): refill it with tile r + S.  A read-then-overwrite by the TMA
             // needs no proxy fence once the read values are in registers.
-            if constexpr (!KV8 || KDIRECT) {
+            // (KV1BAR: refilled with the V half below.)
+            if constexpr (!KV8 || (KDIRECT && !KV1BAR)) {
                 if (rn < nloc) {
                     __syncwarp();
                     if (lane == 0) issue(tmk, 0, rn, k, id_next);
@@ -797,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                 }
             }
 
-            if constexpr (!KV8_APART) {
+            if constexpr (!KV8_APART && !KV1BAR) {
                 if (!dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + k) * 2 + 1]), par)) {
                     fail_r = r;
                     break;
@@ -868,11 +896,16 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                 pv_tile((tv0 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 1 < nvalid ? 0xffff0000u : 0u),
                         (tv0 + 8 < nvalid ? 0x0000ffffu : 0u) | (tv0 + 9 < nvalid ? 0xffff0000u : 0u));
             }
-            // the V half is read: refill it with tile r + S
+            // the V half is read: refill it with tile r + S (KV1BAR: both halves)
             if constexpr (!KV8 || VDIRECT) {
                 if (rn < nloc) {
                     __syncwarp();
-                    if (lane == 0) issue(tmv, 1, rn, k, id_next);
+                    if (lane == 0) {
+                        if constexpr (KV1BAR)
+                            issue_kv(rn, k, id_next);
+                        else
+                            issue(tmv, 1, rn, k, id_next);
+                    }
                 }
             }
             if (++k == S) {
@@ -886,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
             if (lane == 0) dev::flag_status(p.status, kDevWaitTimeout);
             const int last = fail_r + S + 1 < nloc ? fail_r + S + 1 : nloc;
             for (int r = fail_r; r < last; ++r)
-                for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < (KV1BAR ? 1 : 2); ++h)
                     dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + (rr + r) % S) * 2 + h]),
                                            ((rr + r) / S) & 1, 100000000ull);
         }
