@@ -757,10 +757,18 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                     cmx[0] = fmaxf(cmx[0], __shfl_xor_sync(0xffffffffu, cmx[0], off));
                     cmx[1] = fmaxf(cmx[1], __shfl_xor_sync(0xffffffffu, cmx[1], off));
                 }
+                // Paged mode: the reference max of a column moves only when a
+                // tile's max passes it by more than 8 (base-2 units), so most
+                // tiles rescale nothing and the weights stay below 2^8 (any
+                // reference gives the same m, l, o relation; the part, split and
+                // merge folds use the one kept).  The tiled modes keep the true
+                // running max, which their state exposes.
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    const float m_new = fmaxf(m_run[nt][c], cmx[c]);
-                    alpha[nt][c] = dev::exp2_approx(m_run[nt][c] - m_new);
+                    const float m_old = m_run[nt][c];
+                    const float m_new = MODE == kModePaged ? (cmx[c] > m_old + 8.f ? cmx[c] : m_old)
+                                                           : fmaxf(m_old, cmx[c]);
+                    alpha[nt][c] = dev::exp2_approx(m_old - m_new);
                     const float e0 = dev::exp2_approx(x[c] - m_new);
                     const float e1 = dev::exp2_approx(x[c + 2] - m_new);
                     pv[nt][c] = e0;
