@@ -155,3 +155,47 @@ def test_split_launches_with_their_own_workspaces_on_two_streams(cuda_device):
         assert pd.pd_device_status() == 0
         assert torch.equal(oa.view(torch.int16), solo_a.view(torch.int16)), rep
         assert torch.equal(ob.view(torch.int16), solo_b.view(torch.int16)), rep
+
+
+def _rising(lens, D, per_tile_log2, qa, seed):
+    """Scores that rise with the token index by about per_tile_log2 (base 2)
+    per 16-token tile: q is qa on column 0 only, K's column 0 grows with t."""
+    w = W.custom(lens, 8, 2, D, seed=seed)
+    q = np.zeros((len(lens), 8, D), np.float32)
+    q[:, :, 0] = qa
+    w.q = W.bf16_bits(q)
+    k = W.bf16_to_f32(w.k_cache).copy()
+    step = per_tile_log2 / 16 / np.log2(np.e) / w.inv_sqrt_d / qa  # K rise per token
+    bs = w.block_size
+    for s, L in enumerate(lens):
+        for t in range(L):
+            k[w.block_table[s, t // bs], t % bs, :, 0] = t * step
+    w.k_cache = W.bf16_bits(k)
+    return w
+
+
+@pytest.mark.parametrize("per_tile", [7.9, 8.1, 12.0, 30.0])
+@pytest.mark.parametrize("N", [1, 5])
+def test_rising_scores(cuda_device, per_tile, N):
+    # every tile's maximum passes the previous ones: the kernels' reference
+    # max moves at every tile (rise above 8 base-2 units per tile) or every
+    # other tile (just below 8), with weights up to 2^8 in between
+    w = _rising([40, 700, 3000], 128, per_tile, 1.0, seed=47)
+    _check(w, cuda_device, N, 0, f"rising {per_tile}/tile N={N}")
+
+
+@pytest.mark.parametrize("per_tile", [7.9, 12.0])
+def test_rising_scores_fp8(cuda_device, per_tile):
+    w = _rising([40, 700, 3000], 128, per_tile, 16.0, seed=48)
+    k_scale, v_scale = np.float32(0.5), np.float32(0.25)
+    k = W.bf16_to_f32(w.k_cache) / k_scale
+    v = W.bf16_to_f32(w.v_cache) / v_scale
+    w.k_cache = W.e4m3_codes(np.clip(k, -448, 448))
+    w.v_cache = W.e4m3_codes(np.clip(v, -448, 448))
+    w.kv_dtype, w.k_scale, w.v_scale = "e4m3", float(k_scale), float(v_scale)
+    ref = oracle.decode_attn_fp8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale, w.block_table,
+                                 w.context_lens, w.inv_sqrt_d)
+    inp = api.PagedInputs(w, cuda_device)
+    out = api.run_paged(inp, num_splits=5, gqa_pack=0)
+    assert pd.pd_device_status() == 0
+    assert_within_tolerance(api.bf16_to_f64(out), ref, f"rising fp8 {per_tile}/tile")
