@@ -229,8 +229,12 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
 
     // ---- which unit (launch geometry only) ------------------------------------
     const int C = p.cluster;
-    const int part = blockIdx.x % C;
-    int u = blockIdx.x / C;
+    int part = 0;
+    int u = blockIdx.x;
+    if (C > 1) {
+        part = u % C;
+        u /= C;
+    }
     int split = 0;  // paged: the split; fused tiled run: the source (step_tile call)
     if constexpr (MODE == kModePaged) {
         split = u % p.num_splits;
@@ -523,6 +527,8 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     constexpr int GCOLS = HL ? 4 : 8;  // meaningful columns per n-tile
 
     int rr = 0;  // tiles this warp has taken through its ring so far (stage phases)
+    int k_next = 0;         // ring position of the warp's next tile: stage,
+    uint32_t par_next = 0;  // and phase parity
     const int jfirst = C == 1 ? 0 : part;
     const int jstep = C == 1 ? 1 : C;
     for (int j = jfirst; j < V; j += jstep) {
@@ -594,8 +600,8 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         };
         // Ring position of local tile 0: stage k with phase parity par; the
         // tiles take the stages in turn, the parity flipping at each wrap.
-        int k = rr % S;
-        uint32_t par = (rr / S) & 1;
+        int k = k_next;
+        uint32_t par = par_next;
         const int npro = nloc < S ? nloc : S;
         for (int r = 0; r < npro; ++r) {
             const int id = __shfl_sync(0xffffffffu, id_cur, r);
@@ -930,8 +936,12 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
                 for (int h = 0; h < (KV1BAR ? 1 : 2); ++h)
                     dev::mbar_wait_bounded(dev::smem_addr(&bars[(warp * S + (rr + r) % S) * 2 + h]),
                                            ((rr + r) / S) & 1, 100000000ull);
+            k = (rr + nloc) % S;  // as if every tile had gone through
+            par = ((rr + nloc) / S) & 1;
         }
         rr += nloc;
+        k_next = k;
+        par_next = par;
 
         // ---- warp merge of the part (fixed warp order) -----------------------------
         // column sums over the tokens of all lanes of a column
