@@ -622,6 +622,7 @@ int decode_impl(const void *q, const void *k_cache, const void *v_cache, const i
     p.qtiles = qtiles;
     p.cluster = 1;
     p.fd_bs = pd::make_fastdiv(p.block_size);
+    p.fd_kvh = pd::make_fastdiv(p.num_kv_heads);
     p.fd_split = pd::make_fastdiv(num_splits);
     p.max_parts = max_parts_for(dpad, false, kv8, packed_splits);
     p.stages = stages;
@@ -891,6 +892,7 @@ int pd_tiled_step(pd_tiled *t, const void *q, const void *k_pool, const void *v_
     p.qtiles = qtiles;
     p.cluster = 1;
     p.fd_bs = pd::make_fastdiv(p.block_size);
+    p.fd_kvh = pd::make_fastdiv(p.num_kv_heads);
     p.fd_split = pd::make_fastdiv(1);
     p.max_parts = max_parts_for(dpad, true);
     p.stages = stages;
@@ -986,6 +988,7 @@ int tiled_run_fused(pd_tiled *t, const void *q, const pd_tiled_source *sources, 
     p.qtiles = qtiles;
     p.cluster = 1;
     p.fd_bs = pd::make_fastdiv(p.block_size);
+    p.fd_kvh = pd::make_fastdiv(p.num_kv_heads);
     p.fd_split = pd::make_fastdiv(1);
     p.max_parts = max_parts_for(dpad, true);
     p.stages = stages;

@@ -45,8 +45,8 @@ constexpr int kPartTiles = 32;
 // l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1, which is below 2^32
 // because d > 2^(l-1).  Then floor(n / d) = (mulhi(n, m) + n) >> l for every
 // 0 <= n < 2^32, and for n < 2^31 the sum cannot overflow 32 bits.  The
-// kernels use it for the split geometry, whose quotients must equal the
-// plain integer division's.
+// kernels use it for the split geometry and the unit decode, whose quotients
+// must equal the plain integer division's.
 struct FastDiv {
     uint32_t d;  // the divisor
     uint32_t m;  // multiplier
@@ -132,8 +132,9 @@ struct UnitParams {
     // shape
     int num_seqs, num_q_heads, num_kv_heads, group, head_dim, block_size;
     int qtiles;       // CTAs per (s, kvh): ceil(group / rows per CTA)
-    FastDiv fd_split;    // num_splits (paged mode; 1 otherwise), for the split geometry
+    FastDiv fd_split;    // num_splits (paged mode; 1 otherwise): split geometry and unit decode
     FastDiv fd_bs;       // block_size
+    FastDiv fd_kvh;      // num_kv_heads
     int cluster;      // CTAs per unit: 1 (parts in sequence) or max_parts (one part per CTA)
     int max_parts;    // parts a unit's range is cut into at most
     int stages;       // pipeline stages per warp

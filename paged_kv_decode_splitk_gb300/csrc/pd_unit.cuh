@@ -237,8 +237,9 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     }
     int split = 0;  // paged: the split; fused tiled run: the source (step_tile call)
     if constexpr (MODE == kModePaged) {
-        split = u % p.num_splits;
-        u /= p.num_splits;
+        const int un = fast_div(u, p.fd_split);
+        split = u - un * p.num_splits;
+        u = un;
     } else if constexpr (RUN) {
         split = u % p.num_sources;
         u /= p.num_sources;
@@ -250,10 +251,13 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         dev::prefetch_tensormap(tmk);
         dev::prefetch_tensormap(tmv);
     }
-    const int qt = u % p.qtiles;
-    u /= p.qtiles;
-    const int kvh = u % p.num_kv_heads;
-    int s = u / p.num_kv_heads;
+    int qt = 0;
+    if (p.qtiles > 1) {
+        qt = u % p.qtiles;
+        u /= p.qtiles;
+    }
+    int s = fast_div(u, p.fd_kvh);
+    const int kvh = u - s * p.num_kv_heads;
     const int bs = p.block_size;
     const int Lmax = p.max_blocks_per_seq * bs;
     const int tiles_per_block = bs / kTileTokens;
@@ -532,8 +536,8 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     const int jfirst = C == 1 ? 0 : part;
     const int jstep = C == 1 ? 1 : C;
     for (int j = jfirst; j < V; j += jstep) {
-        const int my0 = tile0 + (j * ntiles) / V;
-        const int my1 = tile0 + ((j + 1) * ntiles) / V;
+        const int my0 = V == 1 ? tile0 : tile0 + (j * ntiles) / V;
+        const int my1 = V == 1 ? tile0 + ntiles : tile0 + ((j + 1) * ntiles) / V;
         const int nloc = my1 - my0 > warp ? (my1 - my0 - warp + kWarps - 1) / kWarps : 0;
 
         // Block id of this warp's local tile r of the part (lane-parallel window loads).
