@@ -9,7 +9,8 @@
 //   for the query rows g of the group and the tokens t of the unit's range,
 //     x[g,t] = (q[g] . K[t]) * inv_sqrt_d
 //     m[g]   = max_t x[g,t],  l[g] = sum_t e^(x[g,t]-m[g]),  o[g] = sum_t e^(x[g,t]-m[g]) V[t]
-//   (kept internally in base-2 units: m is max_t x[g,t]*log2(e)).
+//   (kept internally in base-2 units: m is max_t x[g,t]*log2(e), or in paged
+//   mode a reference at most 8 below it, with l and o taken against it).
 //
 // GB300 mapping:
 //   * The unit's range of 16-token tiles is cut into V length-defined parts
@@ -33,7 +34,13 @@
 //     Each warp runs a private ring
 //     of `stages` buffers with separate K and V mbarriers, refilled as soon
 //     as their data has been read, so the next tiles' loads overlap the
-//     current tile's math.
+//     current tile's math (over an FP8 cache at head dim 128, with two stages
+//     per warp, a tile's K and V share one barrier and are refilled together).
+//   * In paged mode a column's reference max moves only when a tile's max
+//     passes it by more than 8 (base 2); every fold uses the reference each
+//     partial carries.  A paged unit of one part skips the part fold and the
+//     cluster hand-off (outside the packed pass it is written straight from
+//     the warp partials).
 //   * Both products run on the tensor cores (mma.sync m16n8k16, BF16 or f16
 //     operands, FP32 accumulate) with the tokens as the M dimension:
 //     S^T[t,g] = K[t,:] q[g,:]^T (the group fills N = 8), then
