@@ -36,8 +36,10 @@ __host__ __device__ inline int splits_used(int context_len, int chunk) {
 }
 
 // Tiles (16 tokens each) a part of a unit's range aims for: the range is cut
-// into ceil(tiles / kPartTiles) parts, at most max_parts.
+// into ceil(tiles / kPartTiles) parts, at most max_parts (the packed pass:
+// kPartTilesPacked).
 constexpr int kPartTiles = 32;
+constexpr int kPartTilesPacked = 24;
 
 // Division by a divisor fixed for a launch, as a multiply-high, an add and a
 // shift (T. Granlund and P. L. Montgomery, "Division by invariant integers

@@ -14,7 +14,8 @@
 //
 // GB300 mapping:
 //   * The unit's range of 16-token tiles is cut into V length-defined parts
-//     (V = clamp(ceil(tiles / kPartTiles), 1, max_parts)).  A CTA of kWarps
+//     (V = clamp(ceil(tiles / PT), 1, max_parts), PT = 32, or 24 in the packed
+//     pass).  A CTA of kWarps
 //     warps takes a part; warp w folds its tiles w, w+kWarps, ... with its own
 //     online-softmax state and the warps merge in warp order.  The parts fold
 //     left to right with pinned rounding, either in one CTA walking them in
@@ -181,6 +182,9 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
     unit_kernel(const __grid_constant__ KvMaps<MODE == kModeTiledRun ? kMaxRunSources : 1> maps,
                 const __grid_constant__ UnitParams p) {
     constexpr int KS = DPAD / 16;      // mma k-steps of K.q^T == m-tiles of V^T.P^T
+    // Tiles a part aims for: the packed pass cuts its (sequence, KV head) units
+    // finer (more of its one wave's CTAs busy; measured 24 against 16 and 32).
+    constexpr int PT = PACKED ? kPartTilesPacked : kPartTiles;
     constexpr int NBOX = DPAD / kBoxCols;                 // BF16 boxes per tile (64 columns each)
     // FP8 cache from head dim 128 up: K's and V's codes go from the (128-byte
     // swizzled) FP8 tiles straight into the mma operands.
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         if (t0 < t1) {
             const int tile0 = t0 / kTileTokens;
             const int ntiles = (t1 + kTileTokens - 1) / kTileTokens - tile0;
-            const int V = max(1, min(p.max_parts, (ntiles + kPartTiles - 1) / kPartTiles));
+            const int V = max(1, min(p.max_parts, (ntiles + PT - 1) / PT));
             const int j = C == 1 ? 0 : part;
             if (j < V) {
                 const int my0 = tile0 + (j * ntiles) / V;
@@ -426,13 +430,13 @@ __global__ void __launch_bounds__(kThreads, CAP4 ? 4 : 0)
         ids_base = (RUN ? p.src_blocks[split] : p.tile_blocks) + static_cast<long long>(s) * p.tile_capacity;
     }
 
-    // 16-token tiles of the range, cut into V parts of about kPartTiles tiles
+    // 16-token tiles of the range, cut into V parts of about PT tiles
     // (at most p.max_parts).  V depends only on the range's own length; the
     // launch decides only where the parts run: all in this CTA one after
     // another (cluster == 1), or one per CTA of a cluster (cluster == max_parts).
     const int tile0 = tok0 / kTileTokens;
     const int ntiles = (tok1 + kTileTokens - 1) / kTileTokens - tile0;
-    const int V = max(1, min(p.max_parts, (ntiles + kPartTiles - 1) / kPartTiles));
+    const int V = max(1, min(p.max_parts, (ntiles + PT - 1) / PT));
     // A rank of a cluster beyond the unit's parts has nothing to do: no peer
     // reads or signals it, so it leaves now and frees its slot.
     if (C > 1 && part >= V) return;
